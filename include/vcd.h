@@ -1,0 +1,130 @@
+/*
+ * vcd.h -- C ABI of the packed (varlen) width-4 depthwise causal convolution
+ * + SiLU, training forward and backward, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one defined on the FlashInfer API pages
+ *   "flashinfer.cake_causal_conv1d_train.cake_causal_conv1d_train_forward"
+ *   "flashinfer.cake_causal_conv1d_train.cake_causal_conv1d_train_backward"
+ * (each entry point below cites the section it follows).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - S tokens (all documents packed back to back), C channels, C % 8 == 0.
+ * - Activations x, y, dy, dx: BF16, [S, C] row-major (channels contiguous),
+ *   device pointers, 16-byte aligned. A [1, S, C] tensor is the same memory.
+ * - weight: [C, 4] row-major, FP32 or BF16, 16-byte aligned; weight[c, 3]
+ *   multiplies the current token, weight[c, 0] the token three back.
+ * - bias: optional [C], FP32 or BF16 (its dtype is independent of weight's),
+ *   16-byte aligned.
+ * - cu_seqlens: int32 [num_docs + 1] device array of document boundaries
+ *   (cu_seqlens[0] == 0, non-decreasing, cu_seqlens[num_docs] == S; a repeated
+ *   value is an empty document). The host never reads it.
+ * - Ownership: the caller owns every buffer. The library allocates nothing,
+ *   frees nothing, reads no device memory on the host and never synchronizes;
+ *   every call only enqueues work on `stream`, so calls can be captured into a
+ *   CUDA graph. Two calls that may run at the same time need two workspaces.
+ * - Errors: arguments are checked before anything is enqueued; on any error
+ *   no output is touched and a vcd_status code is returned. Malformed
+ *   cu_seqlens contents (which the host cannot see) never cause an
+ *   out-of-bounds access; the outputs are then unspecified.
+ * - The functions use the CUDA device that is current on the calling thread.
+ */
+#ifndef VCD_H
+#define VCD_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { VCD_BF16 = 0, VCD_FP32 = 1 } vcd_dtype;
+
+/* Where SiLU' is evaluated in the backward ("silu_grad_preactivation" on the
+ * backward page, Parameters): at the BF16-rounded recomputed preactivation,
+ * or at the unrounded FP32 preactivation (with an FP64 final reduction). */
+typedef enum { VCD_SILU_GRAD_BF16 = 0, VCD_SILU_GRAD_FP32 = 1 } vcd_silu_policy;
+
+typedef enum {
+    VCD_OK = 0,
+    VCD_ERR_INVALID_ARG = 1,          /* bad size, dtype, policy, NULL pointer */
+    VCD_ERR_WORKSPACE_TOO_SMALL = 2,  /* workspace_bytes below the size query */
+    VCD_ERR_MISALIGNED = 3,           /* a pointer breaks its alignment rule   */
+    VCD_ERR_CUDA = 4                  /* a CUDA runtime call failed            */
+} vcd_status;
+
+/* Bytes of forward workspace for (S, C). The forward keeps no counters, so
+ * this is 0 and conv1d_fwd accepts a NULL workspace. (Forward page,
+ * Parameters: workspace.) Returns VCD_OK, or VCD_ERR_INVALID_ARG for S < 0,
+ * C <= 0, C % 8 != 0 or bytes == NULL. */
+int conv1d_fwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
+
+/* Bytes of backward workspace for (S, C): the FP32 partial rows of dweight
+ * and dbias (backward page, Parameters: workspace). A function of (S, C)
+ * alone, the same for every route (bias or not, dtypes, policy) and every
+ * device, so one buffer serves every call of that shape. The kernel writes
+ * every byte it later reads: the buffer needs no zeroing. Same errors as the
+ * forward query. */
+int conv1d_bwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
+
+/* Forward (forward page, Returns):
+ *   y[t, c] = bf16(silu(sum_k weight[c, k] * x[t - 3 + k, c] + bias[c]))
+ * with zero history before each document's first token, FP32 arithmetic,
+ * round-to-nearest-even to BF16.
+ *   x         [S, C] BF16, read.
+ *   weight    [C, 4] of weight_dtype, read.
+ *   cu_seqlens, num_docs   document boundaries, read on the device.
+ *   bias      [C] of bias_dtype or NULL (no bias), read.
+ *   y         [S, C] BF16, written (may not alias x).
+ *   workspace, workspace_bytes   ignored (size query gives 0); may be NULL.
+ *   stream    CUDA stream the kernel is enqueued on.
+ * S == 0 returns VCD_OK without launching. */
+int conv1d_fwd(const void* x, int64_t S, int64_t C,
+               const void* weight, int weight_dtype,
+               const int32_t* cu_seqlens, int64_t num_docs,
+               const void* bias, int bias_dtype,
+               void* y,
+               void* workspace, size_t workspace_bytes,
+               cudaStream_t stream);
+
+/* Backward (backward page, description and Returns). Recomputes the FP32
+ * preactivation from x, evaluates SiLU' at it per `policy`, and writes
+ *   dx[t, c]      = bf16(sum_k weight[c, k] * dpre[t + 3 - k, c])  (same document)
+ *   dweight[c, k] = sum_t dpre[t, c] * x[t - 3 + k, c]             (zero history)
+ *   dbias[c]      = sum_t dpre[t, c]                               (if dbias != NULL)
+ * with dpre = dy * silu'(p). Two launches on `stream`: the main kernel writes
+ * dx and one FP32 partial row per work unit into the workspace, and a reduce
+ * kernel, launched programmatically dependent on it, sums the rows in a fixed
+ * order (FP32 under VCD_SILU_GRAD_BF16, FP64 under VCD_SILU_GRAD_FP32), so the
+ * gradients are bitwise identical for a given (S, C) and route.
+ *   x, dy     [S, C] BF16, read.
+ *   weight, cu_seqlens, num_docs, bias   as in conv1d_fwd (bias must be the
+ *             forward's bias: it enters the preactivation).
+ *   policy    vcd_silu_policy.
+ *   dx        [S, C] BF16, written (may not alias x or dy).
+ *   dweight   [C, 4] of dweight_dtype, written.
+ *   dbias     [C] of dbias_dtype or NULL; non-NULL requires bias != NULL.
+ *   workspace at least conv1d_bwd_workspace_size(S, C) bytes, 16-byte aligned.
+ *   stream    CUDA stream both kernels are enqueued on.
+ * S == 0 writes zero dweight (and dbias) with cudaMemsetAsync and launches
+ * no kernel. */
+int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C,
+               const void* weight, int weight_dtype,
+               const int32_t* cu_seqlens, int64_t num_docs,
+               const void* bias, int bias_dtype,
+               int policy,
+               void* dx, void* dweight, int dweight_dtype,
+               void* dbias, int dbias_dtype,
+               void* workspace, size_t workspace_bytes,
+               cudaStream_t stream);
+
+/* Static description of a vcd_status code (never NULL). */
+const char* conv1d_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VCD_H */

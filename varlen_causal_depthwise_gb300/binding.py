@@ -1,0 +1,161 @@
+"""ctypes binding of ``libvcd.so`` (the C ABI declared in ``include/vcd.h``).
+
+Argument marshalling only: tensors become device pointers, dtypes become
+``vcd_dtype`` codes, the current torch stream becomes the ``cudaStream_t``.
+Every step of the operation runs in the library's CUDA kernels; there is no
+CPU fallback, and a missing library raises instead of degrading.
+"""
+import ctypes
+import os
+
+import torch
+
+VCD_OK = 0
+VCD_ERR_INVALID_ARG = 1
+VCD_ERR_WORKSPACE_TOO_SMALL = 2
+VCD_ERR_MISALIGNED = 3
+VCD_ERR_CUDA = 4
+
+VCD_BF16 = 0
+VCD_FP32 = 1
+POLICIES = {"bf16": 0, "fp32": 1}
+
+_DTYPE = {torch.bfloat16: VCD_BF16, torch.float32: VCD_FP32}
+
+_lib = None
+
+# name -> (restype, argtypes); the same set include/vcd.h declares.
+_vp, _i64, _int, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "conv1d_fwd_workspace_size": (_int, [_i64, _i64, ctypes.POINTER(_sz)]),
+    "conv1d_bwd_workspace_size": (_int, [_i64, _i64, ctypes.POINTER(_sz)]),
+    "conv1d_fwd": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _vp, _vp, _sz,
+                          _vp]),
+    "conv1d_bwd": (_int, [_vp, _vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _int, _vp,
+                          _vp, _int, _vp, _int, _vp, _sz, _vp]),
+    "conv1d_status_string": (ctypes.c_char_p, [_int]),
+}
+
+
+class VcdError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {conv1d_status_string(status)} (status {status})")
+
+
+def library_path():
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvcd.so")
+
+
+def load_library():
+    """Load libvcd.so once; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m varlen_causal_depthwise_gb300.build`"
+                " (or __graft_entry__.build()); there is no CPU fallback")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def conv1d_status_string(status):
+    return load_library().conv1d_status_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != VCD_OK:
+        raise VcdError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dt(t):
+    if t is None:
+        return VCD_FP32
+    if t.dtype not in _DTYPE:
+        raise TypeError(f"unsupported dtype {t.dtype}; FP32 or BF16 expected")
+    return _DTYPE[t.dtype]
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _sc(x):
+    if x.dim() == 3 and x.shape[0] == 1:
+        return int(x.shape[1]), int(x.shape[2])
+    if x.dim() != 2:
+        raise ValueError(f"x must be [S, C] or [1, S, C], got {tuple(x.shape)}")
+    return int(x.shape[0]), int(x.shape[1])
+
+
+def conv1d_fwd_workspace_size(S, C):
+    n = ctypes.c_size_t(0)
+    _check(load_library().conv1d_fwd_workspace_size(int(S), int(C), ctypes.byref(n)),
+           "conv1d_fwd_workspace_size")
+    return n.value
+
+
+def conv1d_bwd_workspace_size(S, C):
+    n = ctypes.c_size_t(0)
+    _check(load_library().conv1d_bwd_workspace_size(int(S), int(C), ctypes.byref(n)),
+           "conv1d_bwd_workspace_size")
+    return n.value
+
+
+def conv1d_fwd(x, weight, cu_seqlens, bias=None, y=None, workspace=None, stream=None):
+    """y = bf16(silu(causal width-4 depthwise conv(x) + bias)), per document.
+
+    x: BF16 CUDA tensor [S, C] or [1, S, C]; weight [C, 4] FP32/BF16;
+    cu_seqlens int32 [num_docs + 1]; bias [C] FP32/BF16 or None.
+    Returns y (allocated when not given)."""
+    lib = load_library()
+    S, C = _sc(x)
+    if y is None:
+        y = torch.empty_like(x)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.conv1d_fwd(_ptr(x), S, C, _ptr(weight), _dt(weight), _ptr(cu_seqlens),
+                        cu_seqlens.numel() - 1, _ptr(bias), _dt(bias), _ptr(y), _ptr(workspace),
+                        nbytes, _stream(stream))
+    _check(st, "conv1d_fwd")
+    return y
+
+
+def conv1d_bwd(x, dy, weight, cu_seqlens, bias=None, policy="bf16", dx=None, dweight=None,
+               dbias=None, workspace=None, stream=None, want_dbias=None):
+    """Gradients of the forward: returns (dx, dweight, dbias or None).
+
+    Output dtypes default to the parameters' dtypes. ``workspace`` (uint8, at
+    least conv1d_bwd_workspace_size(S, C) bytes) is allocated when omitted."""
+    lib = load_library()
+    S, C = _sc(x)
+    if policy not in POLICIES:
+        raise ValueError(f"policy must be 'bf16' or 'fp32', got {policy!r}")
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dweight is None:
+        dweight = torch.empty(C, 4, dtype=weight.dtype, device=x.device)
+    if want_dbias is None:
+        want_dbias = bias is not None
+    if dbias is None and want_dbias:
+        dbias = torch.empty(C, dtype=bias.dtype if bias is not None else torch.float32,
+                            device=x.device)
+    if workspace is None:
+        workspace = torch.empty(conv1d_bwd_workspace_size(S, C), dtype=torch.uint8,
+                                device=x.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib.conv1d_bwd(_ptr(x), _ptr(dy), S, C, _ptr(weight), _dt(weight), _ptr(cu_seqlens),
+                        cu_seqlens.numel() - 1, _ptr(bias), _dt(bias), POLICIES[policy],
+                        _ptr(dx), _ptr(dweight), _dt(dweight), _ptr(dbias), _dt(dbias),
+                        _ptr(workspace), nbytes, _stream(stream))
+    _check(st, "conv1d_bwd")
+    return dx, dweight, dbias
