@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Benchmark of the packed width-4 causal depthwise convolution + SiLU on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the forward (y from x) and the backward (dx, dweight, dbias from x and dy; two
+launches, the second programmatically dependent). The default workload is the
+linear-attention short-conv shape S = 65536 packed tokens, C = 6144 channels
+(q|k|v, 3 x 2048), uniform document lengths in [1, 8192] with 3 empty
+documents, FP32 weight and bias, BF16 x / dy, SiLU' at the BF16-rounded
+preactivation.
+
+Printed JSON (one line, rank 0):
+  value        fwd+bwd achieved HBM GB/s = compulsory bytes (fwd: read x, write y;
+               bwd: read x and dy, write dx, plus the partial rows written and
+               read) / device time, inputs resident in HBM; inputs (805 MB each)
+               exceed the 129 MB L2, so no flush is needed between steps.
+  e2e          the same metric through the public API with pinned host buffers,
+               host->device copies of the step's inputs and device->host copies
+               of its outputs inside the timed region.
+  roofline     backward call (its main kernel dominates the step) against the
+               measured HBM copy bandwidth.
+  cpu_baseline the FP64 oracle (test infrastructure, single-threaded C) timed on
+               a bounded slice of the same workload.
+
+Multi-GPU (torchrun, N > 1): every rank runs an independent replica on its own
+GPU (the operation has no exchange step); value sums the ranks' bytes over the
+slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "fwd/bwd achieved HBM GB/s (% of GB300 peak) and Mtokens/s at S=65536, C=6144"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# ncu DRAM traffic (read + write bytes per launch) of the backward main kernel on
+# the default workload, keyed by the SHA-256 of the kernel sources it was taken
+# on; a changed kernel reports traffic null until it is profiled again.
+NCU_TRAFFIC = {}
+KERNEL_SOURCES = ["varlen_causal_depthwise_gb300/csrc/vcd_bwd.cu",
+                  "varlen_causal_depthwise_gb300/csrc/vcd_device.cuh",
+                  "varlen_causal_depthwise_gb300/csrc/vcd_plan.h"]
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.window = None    # (t0, t1) wall-clock seconds of the timed region
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                clk, cmax = float(f[2]), float(f[3])
+            except (ValueError, IndexError):
+                continue
+            if self.window and not (self.window[0] - 0.25 <= ts <= self.window[1] + 0.25):
+                continue
+            sm.append(clk)
+            mx.append(cmax)
+            for n, v in zip(names, f[6:10]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def compulsory_bytes(S, C, partial_bytes):
+    E = S * C
+    fwd = 4 * E
+    bwd = 6 * E + 2 * partial_bytes
+    return fwd, bwd
+
+
+def run_ours(args):
+    import torch.distributed as dist
+
+    import varlen_causal_depthwise_gb300 as vcd
+    from varlen_causal_depthwise_gb300 import synth
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    recipe = synth.RECIPES[args.config]
+    w = synth.make(args.config, device=dev)
+    S, C = w.S, w.C
+    policy = recipe.policies[0]
+    nws = vcd.conv1d_bwd_workspace_size(S, C)
+    wsp = torch.empty(nws, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(w.x)
+    dx = torch.empty_like(w.x)
+    dW = torch.empty(C, 4, dtype=w.weight.dtype, device=dev)
+    dB = None if w.bias is None else torch.empty(C, dtype=w.bias.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        vcd.conv1d_fwd(w.x, w.weight, w.cu_seqlens, w.bias, y=y, stream=stream)
+
+    def bwd():
+        vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, policy, dx=dx, dweight=dW,
+                       dbias=dB, workspace=wsp, stream=stream)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with ClockSampler(local) as clk:
+        time.sleep(0.5)                 # let the sampler start
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        wall0 = time.time()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            bwd()
+            ev[i][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        clk.mark(wall0, time.time())
+        if ws > 1:
+            dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end: pinned host buffers through the public API ----
+    hx = w.x.cpu().pin_memory()
+    hdy = w.dy.cpu().pin_memory()
+    hW = w.weight.cpu().pin_memory()
+    hb = None if w.bias is None else w.bias.cpu().pin_memory()
+    hcu = w.cu_seqlens.cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory()
+    hdW = torch.empty(dW.shape, dtype=dW.dtype).pin_memory()
+    hdB = None if dB is None else torch.empty(dB.shape, dtype=dB.dtype).pin_memory()
+    h2d = [(hx, w.x), (hdy, w.dy), (hW, w.weight), (hcu, w.cu_seqlens)]
+    if hb is not None:
+        h2d.append((hb, w.bias))
+    d2h = [(y, hy), (dx, hdx), (dW, hdW)] + ([(dB, hdB)] if dB is not None else [])
+    h2d_bytes = sum(h.numel() * h.element_size() for h, _ in h2d)
+    d2h_bytes = sum(h.numel() * h.element_size() for _, h in d2h)
+
+    def e2e_step():
+        for h, d in h2d:
+            d.copy_(h, non_blocking=True)
+        fwd()
+        bwd()
+        for d, h in d2h:
+            h.copy_(d, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    Ke = max(3, min(K, 10))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    fwd_b, bwd_b = compulsory_bytes(S, C, nws)
+    step_b = fwd_b + bwd_b
+    ms_step = total_ms / K
+    peak, peak_kind = measured_peak()
+    fwd_us = 1e3 * statistics.median(fwd_ms)
+    bwd_us = 1e3 * statistics.median(bwd_ms)
+    bwd_mean_us = 1e3 * statistics.mean(bwd_ms)
+    clocks = clk.summary()
+
+    def direction(nbytes, us):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"us_median": round(us, 2), "gbs": round(gbs, 1),
+                "frac_of_measured": round(gbs / peak, 4),
+                "frac_of_8tbs_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+                "mtokens_per_s": round(S / (us * 1e-6) / 1e6, 2),
+                "bytes": nbytes}
+
+    value = ws * step_b / (ms_step * 1e-3) / 1e9
+    sha = kernel_sha()
+    tr = NCU_TRAFFIC.get(sha)
+    bwd_achieved = bwd_b / (bwd_mean_us * 1e-6) / 1e9
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{args.config}: S={S}, C={C}, {w.num_docs} docs, "
+                               f"weight {str(w.weight.dtype)[6:]}, "
+                               f"bias {'none' if w.bias is None else str(w.bias.dtype)[6:]}, "
+                               f"SiLU' policy {policy}, BF16 x/dy/y/dx",
+                   "S": S, "C": C, "num_docs": w.num_docs, "policy": policy,
+                   "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (no flush needed)"},
+        "detail": {"fwd": direction(fwd_b, fwd_us), "bwd": direction(bwd_b, bwd_us),
+                   "step": {"gbs": round(step_b / (ms_step * 1e-3) / 1e9, 1),
+                            "mtokens_per_s": round(S / (ms_step * 1e-3) / 1e6, 2),
+                            "frac_of_measured": round(step_b / (ms_step * 1e-3) / 1e9 / peak, 4)}},
+        "roofline": {"kernel": "conv1d_bwd (main + dependent reduce)", "bound": "hbm",
+                     "achieved": round(bwd_achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(bwd_achieved / peak, 4),
+                     "traffic": tr, "algorithmic_bytes": bwd_b},
+        "e2e": {"value": round(ws * step_b / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h_bytes},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "kernel_sha": sha,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, policy, args.cpu_tokens)
+    if ws > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def oracle_slice(w, tokens):
+    """The first `tokens` tokens of the workload as a CPU problem of its own
+    (documents cut at the slice end)."""
+    import numpy as np
+
+    from varlen_causal_depthwise_gb300 import synth
+
+    n = min(tokens, w.S)
+    lens, tot = [], 0
+    for L in w.lengths:
+        if tot >= n:
+            break
+        take = min(L, n - tot)
+        lens.append(take)
+        tot += take
+    cu = synth.cu_from_lengths(lens)
+    x = w.x[:n].cpu()
+    dy = w.dy[:n].cpu()
+    return x, dy, w.weight.cpu(), None if w.bias is None else w.bias.cpu(), cu, n, np
+
+
+def cpu_baseline(w, policy, tokens):
+    import oracle
+
+    x, dy, W, b, cu, n, _ = oracle_slice(w, tokens)
+    t0 = time.perf_counter()
+    oracle.fwd(x, W, cu, b)
+    oracle.bwd(x, dy, W, cu, b, policy)
+    dt = time.perf_counter() - t0
+    fwd_b, bwd_b = compulsory_bytes(n, w.C, 0)
+    return {"value": round((fwd_b + bwd_b) / dt / 1e9, 5), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"first {n} tokens x all {w.C} channels of the same workload, "
+                      f"fwd + bwd ({policy}), single-threaded FP64 C"}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    from varlen_causal_depthwise_gb300 import synth
+    import oracle
+
+    recipe = synth.RECIPES[args.config]
+    policy = recipe.policies[0]
+    # inputs drawn on the GPU when there is one (faster; the oracle still runs on
+    # the host cores), else on the CPU
+    w = synth.make(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
+    x, dy, W, b, cu, n, _ = oracle_slice(w, args.ref_tokens)
+    del w.x, w.dy
+    for _ in range(args.warmup):
+        oracle.fwd(x[:8], W, synth.cu_from_lengths([8]), b)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.fwd(x, W, cu, b)
+        oracle.bwd(x, dy, W, cu, b, policy)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.median(times)
+    fwd_b, bwd_b = compulsory_bytes(n, w.C, 0)
+    v = round((fwd_b + bwd_b) / dt / 1e9, 5)
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": f"{args.config}: S={w.S}, C={w.C} (bounded slice: first {n} "
+                                  f"tokens per step)", "S": w.S, "C": w.C},
+           "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                            "sample": f"first {n} tokens x {w.C} channels, fwd + bwd ({policy})"},
+           "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="linattn",
+                    choices=["tiny", "mid", "linattn", "boundary", "large"])
+    ap.add_argument("--cpu-tokens", type=int, default=1536,
+                    help="tokens of the workload the CPU-baseline oracle leg processes")
+    ap.add_argument("--ref-tokens", type=int, default=96,
+                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

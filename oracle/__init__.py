@@ -48,11 +48,11 @@ def _declare(lib):
     lib.vcd_oracle_fwd_at.argtypes = [_i64, _i64, _U16, _D, _D, _I32, _i64, _i64, _I64, _I64,
                                       _D, _D]
     lib.vcd_oracle_bwd.argtypes = [_i64, _i64, _U16, _U16, _D, _D, _I32, _i64, ctypes.c_int,
-                                   _D, _D, _D, _D]
+                                   _D, _D, _D, _D, _D, _D]
     lib.vcd_oracle_bwd_dx_at.argtypes = [_i64, _i64, _U16, _U16, _D, _D, _I32, _i64,
                                          ctypes.c_int, _i64, _I64, _I64, _D, _D]
     lib.vcd_oracle_bwd_params_at.argtypes = [_i64, _i64, _U16, _U16, _D, _D, _I32, _i64,
-                                             ctypes.c_int, _i64, _I64, _D, _D]
+                                             ctypes.c_int, _i64, _I64, _D, _D, _D, _D]
     for name in ("vcd_oracle_round_bf16", "vcd_oracle_silu", "vcd_oracle_silu_grad"):
         getattr(lib, name).argtypes = [ctypes.c_double]
         getattr(lib, name).restype = ctypes.c_double
@@ -136,8 +136,9 @@ def fwd_at(x, weight, cu_seqlens, ts, cs, bias=None, lib=None):
     return y, a
 
 
-def bwd(x, dy, weight, cu_seqlens, bias=None, policy="bf16", lib=None):
-    """Full backward. Returns (dx, dx_allowance, dweight [C,4], dbias [C] or None)."""
+def bwd(x, dy, weight, cu_seqlens, bias=None, policy="bf16", lib=None, magnitudes=False):
+    """Full backward. Returns (dx, dx_allowance, dweight [C,4], dbias [C] or None),
+    plus (dweight_mag, dbias_mag) -- the sums of |term| -- with magnitudes=True."""
     lib = lib or load()
     x, S, C = _shape(x)
     dy, _, _ = _shape(dy)
@@ -147,10 +148,14 @@ def bwd(x, dy, weight, cu_seqlens, bias=None, policy="bf16", lib=None):
     a = np.zeros((S, C), np.float64)
     dw = np.zeros((C, 4), np.float64)
     db = np.zeros(C, np.float64) if bias is not None else None
+    mw = np.zeros((C, 4), np.float64)
+    mb = np.zeros(C, np.float64)
     rc = lib.vcd_oracle_bwd(S, C, _p(xb, _U16), _p(gb, _U16), _p(w, _D), _p(b, _D),
                             _p(cu, _I32), len(cu) - 1, POLICY[policy], _p(dx, _D), _p(a, _D),
-                            _p(dw, _D), _p(db, _D))
+                            _p(dw, _D), _p(db, _D), _p(mw, _D), _p(mb, _D))
     _check(rc, "bwd")
+    if magnitudes:
+        return dx, a, dw, db, mw, (mb if bias is not None else None)
     return dx, a, dw, db
 
 
@@ -171,8 +176,10 @@ def bwd_dx_at(x, dy, weight, cu_seqlens, ts, cs, bias=None, policy="bf16", lib=N
     return dx, a
 
 
-def bwd_params_at(x, dy, weight, cu_seqlens, cs, bias=None, policy="bf16", lib=None):
-    """dweight [n,4] and dbias [n] (None without bias) for the listed channels."""
+def bwd_params_at(x, dy, weight, cu_seqlens, cs, bias=None, policy="bf16", lib=None,
+                  magnitudes=False):
+    """dweight [n,4] and dbias [n] (None without bias) for the listed channels,
+    plus their magnitude sums with magnitudes=True."""
     lib = lib or load()
     x, S, C = _shape(x)
     dy, _, _ = _shape(dy)
@@ -181,10 +188,15 @@ def bwd_params_at(x, dy, weight, cu_seqlens, cs, bias=None, policy="bf16", lib=N
     cs = _i64a(cs)
     dw = np.zeros((len(cs), 4), np.float64)
     db = np.zeros(len(cs), np.float64) if bias is not None else None
+    mw = np.zeros((len(cs), 4), np.float64)
+    mb = np.zeros(len(cs), np.float64)
     rc = lib.vcd_oracle_bwd_params_at(S, C, _p(xb, _U16), _p(gb, _U16), _p(w, _D), _p(b, _D),
                                       _p(cu, _I32), len(cu) - 1, POLICY[policy], len(cs),
-                                      _p(cs, _I64), _p(dw, _D), _p(db, _D))
+                                      _p(cs, _I64), _p(dw, _D), _p(db, _D), _p(mw, _D),
+                                      _p(mb, _D))
     _check(rc, "bwd_params_at")
+    if magnitudes:
+        return dw, db, mw, (mb if bias is not None else None)
     return dw, db
 
 

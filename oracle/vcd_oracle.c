@@ -293,17 +293,30 @@ static int dx_elem(const problem* P, int64_t t, int64_t c, int policy, double* d
     return ORC_OK;
 }
 
-static int params_channel(const problem* P, int64_t c, int policy, double* dw4, double* db) {
+/* dweight [4] and dbias of channel c; with non-NULL mag4 / magb also the sums
+ * of the magnitudes of their terms, sum_t |dpre * xm| and sum_t |dpre|. */
+static int params_channel(const problem* P, int64_t c, int policy, double* dw4, double* db,
+                          double* mag4, double* magb) {
     if (c < 0 || c >= P->C) return ORC_BAD;
     nsum acc[4] = {{0, 0}, {0, 0}, {0, 0}, {0, 0}};
     nsum accb = {0.0, 0.0};
+    double m[4] = {0, 0, 0, 0}, mb = 0.0;
     for (int64_t t = 0; t < P->S; ++t) {
         double d = dpre_at(P, t, c, policy, NULL);
-        for (int k = 0; k < 4; ++k) nsum_add(&acc[k], d * xm(P, t, t - 3 + k, c));
+        for (int k = 0; k < 4; ++k) {
+            double term = d * xm(P, t, t - 3 + k, c);
+            nsum_add(&acc[k], term);
+            m[k] += fabs(term);
+        }
         nsum_add(&accb, d);
+        mb += fabs(d);
     }
-    for (int k = 0; k < 4; ++k) dw4[k] = nsum_get(&acc[k]);
+    for (int k = 0; k < 4; ++k) {
+        dw4[k] = nsum_get(&acc[k]);
+        if (mag4) mag4[k] = m[k];
+    }
     if (db) *db = nsum_get(&accb);
+    if (magb) *magb = mb;
     return ORC_OK;
 }
 
@@ -315,17 +328,21 @@ static int check_bwd(const problem* P, int policy) {
 }
 
 /* Full backward: dx [S, C] (+ allowance), dweight [C, 4], dbias [C]
- * (dbias may be NULL). S == 0 gives zero gradients (B, Returns). */
+ * (dbias may be NULL), and optionally the magnitude sums of the gradients'
+ * terms (dweight_mag [C, 4], dbias_mag [C]; NULL to skip). S == 0 gives zero
+ * gradients (B, Returns). */
 int vcd_oracle_bwd(int64_t S, int64_t C, const uint16_t* x, const uint16_t* dy, const double* w,
                    const double* b, const int32_t* cu, int64_t num_docs, int policy, double* dx,
-                   double* dx_allow, double* dweight, double* dbias) {
+                   double* dx_allow, double* dweight, double* dbias, double* dweight_mag,
+                   double* dbias_mag) {
     problem P = {S, C, num_docs, x, dy, w, b, cu};
     if (check_bwd(&P, policy) != ORC_OK || !dweight || (S > 0 && !dx)) return ORC_BAD;
     for (int64_t t = 0; t < S; ++t)
         for (int64_t c = 0; c < C; ++c)
             dx_elem(&P, t, c, policy, &dx[t * C + c], dx_allow ? &dx_allow[t * C + c] : NULL);
     for (int64_t c = 0; c < C; ++c)
-        params_channel(&P, c, policy, &dweight[c * 4], dbias ? &dbias[c] : NULL);
+        params_channel(&P, c, policy, &dweight[c * 4], dbias ? &dbias[c] : NULL,
+                       dweight_mag ? &dweight_mag[c * 4] : NULL, dbias_mag ? &dbias_mag[c] : NULL);
     return ORC_OK;
 }
 
@@ -341,15 +358,19 @@ int vcd_oracle_bwd_dx_at(int64_t S, int64_t C, const uint16_t* x, const uint16_t
     return ORC_OK;
 }
 
-/* dweight / dbias for a list of channels: dweight [n, 4], dbias [n]. */
+/* dweight / dbias for a list of channels: dweight [n, 4], dbias [n], and
+ * optionally their magnitude sums (same shapes; NULL to skip). */
 int vcd_oracle_bwd_params_at(int64_t S, int64_t C, const uint16_t* x, const uint16_t* dy,
                              const double* w, const double* b, const int32_t* cu,
                              int64_t num_docs, int policy, int64_t n, const int64_t* cs,
-                             double* dweight, double* dbias) {
+                             double* dweight, double* dbias, double* dweight_mag,
+                             double* dbias_mag) {
     problem P = {S, C, num_docs, x, dy, w, b, cu};
     if (check_bwd(&P, policy) != ORC_OK || n < 0) return ORC_BAD;
     for (int64_t i = 0; i < n; ++i)
-        if (params_channel(&P, cs[i], policy, &dweight[i * 4], dbias ? &dbias[i] : NULL) != ORC_OK)
+        if (params_channel(&P, cs[i], policy, &dweight[i * 4], dbias ? &dbias[i] : NULL,
+                           dweight_mag ? &dweight_mag[i * 4] : NULL,
+                           dbias_mag ? &dbias_mag[i] : NULL) != ORC_OK)
             return ORC_BAD;
     return ORC_OK;
 }

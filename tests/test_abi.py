@@ -1,0 +1,122 @@
+"""The C ABI library loads on any host, exports every entry point include/vcd.h
+declares, and rejects bad arguments before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import varlen_causal_depthwise_gb300 as vcd
+from varlen_causal_depthwise_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vcd.h")
+
+
+def declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(conv1d_\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(binding.library_path()):
+        from varlen_causal_depthwise_gb300 import build
+        build.build()
+    return binding.load_library()
+
+
+def test_header_declares_the_entry_points():
+    assert declared() == sorted(binding.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert vcd.conv1d_status_string(0) == "ok"
+    for s in range(1, 5):
+        assert vcd.conv1d_status_string(s) not in ("ok", "unknown status")
+    assert vcd.conv1d_status_string(99) == "unknown status"
+
+
+def test_workspace_queries(lib):
+    assert vcd.conv1d_fwd_workspace_size(65536, 6144) == 0
+    assert vcd.conv1d_bwd_workspace_size(0, 256) == 0
+    n = vcd.conv1d_bwd_workspace_size(65536, 6144)
+    assert n > 0 and n % 16 == 0
+    # one FP32 row of 128 channels x 5 values per work unit, about one unit per warp
+    assert n <= 2432 * 128 * 5 * 4
+    for bad in ((-1, 8), (8, 0), (8, 12)):
+        with pytest.raises(vcd.VcdError):
+            vcd.conv1d_bwd_workspace_size(*bad)
+
+
+def _fwd(lib, **kw):
+    a = dict(x=16, S=4, C=8, w=16, wd=1, cu=16, nd=1, b=None, bd=1, y=32, ws=None, wsb=0)
+    a.update(kw)
+    return lib.conv1d_fwd(a["x"], a["S"], a["C"], a["w"], a["wd"], a["cu"], a["nd"], a["b"],
+                          a["bd"], a["y"], a["ws"], a["wsb"], None)
+
+
+def _bwd(lib, **kw):
+    a = dict(x=16, dy=48, S=4, C=8, w=16, wd=1, cu=16, nd=1, b=None, bd=1, pol=0, dx=32,
+             dw=64, dwd=1, db=None, dbd=1, ws=80, wsb=1 << 20)
+    a.update(kw)
+    return lib.conv1d_bwd(a["x"], a["dy"], a["S"], a["C"], a["w"], a["wd"], a["cu"], a["nd"],
+                          a["b"], a["bd"], a["pol"], a["dx"], a["dw"], a["dwd"], a["db"], a["dbd"],
+                          a["ws"], a["wsb"], None)
+
+
+# Fake, never dereferenced addresses: every case below must fail validation
+# before the library reaches the CUDA runtime.
+@pytest.mark.parametrize("kw,status", [
+    (dict(C=12), binding.VCD_ERR_INVALID_ARG),          # C % 8 != 0
+    (dict(C=0), binding.VCD_ERR_INVALID_ARG),
+    (dict(S=-1), binding.VCD_ERR_INVALID_ARG),
+    (dict(nd=0), binding.VCD_ERR_INVALID_ARG),          # tokens but no documents
+    (dict(wd=7), binding.VCD_ERR_INVALID_ARG),
+    (dict(x=None), binding.VCD_ERR_INVALID_ARG),
+    (dict(y=None), binding.VCD_ERR_INVALID_ARG),
+    (dict(y=16), binding.VCD_ERR_INVALID_ARG),          # y aliases x
+    (dict(x=18), binding.VCD_ERR_MISALIGNED),
+    (dict(w=20), binding.VCD_ERR_MISALIGNED),
+    (dict(b=24, bd=0), binding.VCD_ERR_MISALIGNED),
+    (dict(y=40), binding.VCD_ERR_MISALIGNED),
+])
+def test_fwd_rejects(lib, kw, status):
+    assert _fwd(lib, **kw) == status
+
+
+def test_fwd_empty_sequence_launches_nothing(lib):
+    assert _fwd(lib, S=0, nd=0, x=None, y=None, cu=16) == binding.VCD_OK
+    assert _fwd(lib, S=0, nd=3) == binding.VCD_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(C=4), binding.VCD_ERR_INVALID_ARG),
+    (dict(pol=2), binding.VCD_ERR_INVALID_ARG),
+    (dict(db=96), binding.VCD_ERR_INVALID_ARG),         # dbias without bias
+    (dict(dw=None), binding.VCD_ERR_INVALID_ARG),
+    (dict(dwd=5), binding.VCD_ERR_INVALID_ARG),
+    (dict(dx=16), binding.VCD_ERR_INVALID_ARG),         # dx aliases x
+    (dict(dx=48), binding.VCD_ERR_INVALID_ARG),         # dx aliases dy
+    (dict(dy=None), binding.VCD_ERR_INVALID_ARG),
+    (dict(dy=50), binding.VCD_ERR_MISALIGNED),
+    (dict(dw=66), binding.VCD_ERR_MISALIGNED),          # FP32 dweight needs 4 bytes
+    (dict(ws=None), binding.VCD_ERR_WORKSPACE_TOO_SMALL),
+    (dict(wsb=16), binding.VCD_ERR_WORKSPACE_TOO_SMALL),
+    (dict(ws=88), binding.VCD_ERR_MISALIGNED),
+])
+def test_bwd_rejects(lib, kw, status):
+    assert _bwd(lib, **kw) == status
+
+
+def test_binding_refuses_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "libvcd.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        binding.load_library()

@@ -1,0 +1,297 @@
+"""Parity of the CUDA library (through its C ABI) with the FP64 oracle.
+
+Small cases compare every output element; the five specified workloads run at
+full size in the same launch configuration the benchmark times and are checked
+on sampled elements (document starts, work-unit boundaries, the last tokens,
+random positions) and on a sample of channels' dweight / dbias.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import varlen_causal_depthwise_gb300 as vcd
+from varlen_causal_depthwise_gb300 import synth
+from _check import bf16_close, grads_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+REPORT = {}
+
+
+def _np(t):
+    return t.detach().double().cpu().numpy()
+
+
+def run_fwd(w):
+    return vcd.conv1d_fwd(w.x, w.weight, w.cu_seqlens, w.bias)
+
+
+def run_bwd(w, policy, dweight_dtype=None, dbias_dtype=None, workspace=None):
+    C = w.C
+    dW = torch.empty(C, 4, dtype=dweight_dtype or w.weight.dtype, device=DEV)
+    dB = None
+    if w.bias is not None:
+        dB = torch.empty(C, dtype=dbias_dtype or w.bias.dtype, device=DEV)
+    return vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, policy, dweight=dW,
+                          dbias=dB, workspace=workspace)
+
+
+def full_check(wc, policies, what):
+    """Every element against the full oracle; wc lives on the CPU."""
+    w = wc.to(DEV)
+    y = run_fwd(w)
+    torch.cuda.synchronize()
+    ry, ay = oracle.fwd(wc.x, wc.weight, wc.cu_seqlens, wc.bias)
+    REPORT[f"{what} y strict"] = bf16_close(_np(y), ry, ay, f"{what} y")
+    for pol in policies:
+        rdx, adx, rdw, rdb, mdw, mdb = oracle.bwd(wc.x, wc.dy, wc.weight, wc.cu_seqlens, wc.bias,
+                                                  pol, magnitudes=True)
+        # outputs in the parameters' dtypes (BF16 -> 1-ulp rule) and in FP32 (rel-L2)
+        for dwt in {w.weight.dtype, torch.float32}:
+            dx, dW, dB = run_bwd(w, pol, dwt, torch.float32 if dwt == torch.float32 else None)
+            torch.cuda.synchronize()
+            REPORT[f"{what} {pol} dx strict"] = bf16_close(_np(dx), rdx, adx, f"{what} {pol} dx")
+            bf_b = dB is not None and dB.dtype == torch.bfloat16
+            grads_close(_np(dW), None if dB is None else _np(dB), rdw, rdb, pol,
+                        dW.dtype == torch.bfloat16, bf_b, f"{what} {pol}", mdw, mdb, wc.S)
+
+
+# ------------------------------------------------------------- small, full --
+
+@pytest.mark.parametrize("name,S,C", [
+    ("tiny", None, None),
+    ("mid", 2048, 264),
+    ("linattn", 3000, 384),
+    ("boundary", 2000, 1032),
+    ("large", 2500, 512),
+])
+def test_recipes_scaled_full(name, S, C):
+    wc = synth.make(name, S=S, C=C)
+    full_check(wc, synth.RECIPES[name].policies, name)
+
+
+@pytest.mark.parametrize("lengths", [
+    [1], [2], [3], [5], [1] * 40, [0, 0, 7, 0], [0] * 5 + [33] + [0] * 5,
+    [4, 1, 1, 1, 9, 0, 2, 3], list(range(0, 40)),
+])
+@pytest.mark.parametrize("C", [8, 16, 264])
+def test_edge_documents(lengths, C):
+    S = sum(lengths)
+    wc = synth.custom(S, C, lengths, seed=S * 31 + C)
+    full_check(wc, ("bf16", "fp32"), f"edge S={S} C={C}")
+
+
+@pytest.mark.parametrize("S,C,seed", [(1000, 8, 1), (1021, 1032, 2), (4099, 136, 3),
+                                      (700, 2056, 4)])
+def test_ragged_units(S, C, seed):
+    """Sizes whose work units end mid-batch and whose channel columns are partial."""
+    rng = np.random.default_rng(seed)
+    lengths = synth.doc_lengths(("uniform", 0, 97, 2), S, rng)
+    wc = synth.custom(S, C, lengths, seed=seed, weight_dtype=torch.bfloat16,
+                      bias_dtype=torch.bfloat16)
+    full_check(wc, ("bf16", "fp32"), f"ragged S={S} C={C}")
+
+
+def test_no_bias_and_mixed_dtypes():
+    for wdt, bdt in [(torch.float32, None), (torch.bfloat16, torch.float32),
+                     (torch.float32, torch.bfloat16), (torch.bfloat16, None)]:
+        wc = synth.custom(300, 40, [100, 0, 150, 50], seed=7, weight_dtype=wdt, bias_dtype=bdt)
+        full_check(wc, ("bf16", "fp32"), f"dtypes {wdt} {bdt}")
+
+
+# ------------------------------------------------------ full size, sampled --
+
+def _unit_edges(S, C, vec):
+    """Token positions next to work-unit edges (sample selection only)."""
+    ncols = -(-(C // vec) // 32)
+    rows = max(1, min(2432 // ncols, -(-S // 64)))
+    L = -(-S // rows)
+    edges = np.arange(0, S, L)
+    return np.unique(np.clip(np.concatenate([edges + d for d in (-4, -3, -1, 0, 1, 2, 3)]), 0, S - 1))
+
+
+def sample_points(w, n_random, rng):
+    S, C = w.S, w.C
+    cu = w.cu_seqlens.cpu().numpy()
+    starts = np.unique(cu[:-1][cu[:-1] < S])
+    special = np.concatenate([
+        starts[:40], starts[-10:], (starts[:20] + 1), (starts[:20] + 2), (starts[:20] + 3),
+        _unit_edges(S, C, 8), _unit_edges(S, C, 4), [0, 1, 2, S - 3, S - 2, S - 1]])
+    special = np.unique(np.clip(special, 0, S - 1))
+    ch = np.unique(np.concatenate([[0, 1, 7, 8, C - 8, C - 1, 127, 128, 255, 256],
+                                   rng.integers(0, C, 6)]))
+    ch = ch[ch < C]
+    ts = np.concatenate([np.repeat(special, len(ch)), rng.integers(0, S, n_random)])
+    cs = np.concatenate([np.tile(ch, len(special)), rng.integers(0, C, n_random)])
+    return ts, cs
+
+
+def sample_channels(C, rng, n=24):
+    ch = np.concatenate([[0, 1, 4, 7, 8, 127, 128, 255, 256, C - 5, C - 1], rng.integers(0, C, n)])
+    return np.unique(ch[ch < C])
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid", "linattn", "boundary", "large"])
+def test_recipes_full_size_sampled(name):
+    rng = np.random.default_rng(123)
+    w = synth.make(name, device=DEV)
+    y = run_fwd(w)
+    torch.cuda.synchronize()
+    xc, dyc = w.x.cpu(), w.dy.cpu()
+    wgt = w.weight.cpu()
+    bias = None if w.bias is None else w.bias.cpu()
+    cu = w.cu_seqlens.cpu()
+    ts, cs = sample_points(w, 20000, rng)
+    ry, ay = oracle.fwd_at(xc, wgt, cu, ts, cs, bias)
+    yg = y[torch.from_numpy(ts).to(DEV), torch.from_numpy(cs).to(DEV)]
+    REPORT[f"{name} full y strict"] = bf16_close(_np(yg), ry, ay, f"{name} y")
+    del y
+    chans = sample_channels(w.C, rng)
+    for pol in synth.RECIPES[name].policies:
+        for dwt in {w.weight.dtype, torch.float32}:
+            dx, dW, dB = run_bwd(w, pol, dwt, torch.float32 if dwt == torch.float32 else None)
+            torch.cuda.synchronize()
+            rdx, adx = oracle.bwd_dx_at(xc, dyc, wgt, cu, ts, cs, bias, pol)
+            dxg = dx[torch.from_numpy(ts).to(DEV), torch.from_numpy(cs).to(DEV)]
+            REPORT[f"{name} full {pol} dx strict"] = bf16_close(_np(dxg), rdx, adx,
+                                                                f"{name} {pol} dx")
+            del dx
+            rdw, rdb, mdw, mdb = oracle.bwd_params_at(xc, dyc, wgt, cu, chans, bias, pol,
+                                                      magnitudes=True)
+            gdw = _np(dW)[chans]
+            gdb = None if dB is None else _np(dB)[chans]
+            grads_close(gdw, gdb, rdw, rdb, pol, dW.dtype == torch.bfloat16,
+                        dB is not None and dB.dtype == torch.bfloat16, f"{name} {pol}", mdw, mdb,
+                        w.S)
+    del w
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------- properties --
+
+@pytest.mark.parametrize("name", ["linattn", "boundary"])
+def test_gradients_bitwise_reproducible(name):
+    """Same (S, C, route) -> identical bits, whatever the workspace held before."""
+    w = synth.make(name, device=DEV)
+    for pol in synth.RECIPES[name].policies:
+        ws = torch.empty(vcd.conv1d_bwd_workspace_size(w.S, w.C), dtype=torch.uint8, device=DEV)
+        ws.fill_(0)
+        a = run_bwd(w, pol, torch.float32, torch.float32 if w.bias is not None else None, ws)
+        ws.fill_(0xFF)                     # NaN patterns: the kernel must overwrite them
+        b = run_bwd(w, pol, torch.float32, torch.float32 if w.bias is not None else None, ws)
+        c = run_bwd(w, pol, torch.float32, torch.float32 if w.bias is not None else None)
+        torch.cuda.synchronize()
+        for u, v, z in zip(a, b, c):
+            if u is None:
+                continue
+            assert torch.equal(u.view(torch.int16) if u.dtype == torch.bfloat16 else u.view(torch.int32),
+                               v.view(torch.int16) if v.dtype == torch.bfloat16 else v.view(torch.int32))
+            assert torch.equal(u, z)
+
+
+def _guarded(n, dtype, guard=64, fill=None):
+    buf = torch.empty(n + 2 * guard, dtype=dtype, device=DEV)
+    buf.view(torch.uint8).fill_(0xA5 if fill is None else fill)
+    return buf, buf[guard:guard + n]
+
+
+def test_outputs_stay_in_bounds():
+    """Sentinel guard bands around every output and the workspace survive."""
+    wc = synth.custom(1500, 264, [700, 0, 500, 300], seed=3, bias_dtype=torch.float32)
+    w = wc.to(DEV)
+    S, C = w.S, w.C
+    ybuf, y = _guarded(S * C, torch.bfloat16)
+    vcd.conv1d_fwd(w.x, w.weight, w.cu_seqlens, w.bias, y=y.view(S, C))
+    dxbuf, dx = _guarded(S * C, torch.bfloat16)
+    dwbuf, dW = _guarded(C * 4, torch.float32)
+    dbbuf, dB = _guarded(C, torch.float32)
+    nws = vcd.conv1d_bwd_workspace_size(S, C)
+    wsbuf, ws = _guarded(nws, torch.uint8)
+    vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, "bf16", dx=dx.view(S, C),
+                   dweight=dW.view(C, 4), dbias=dB, workspace=ws)
+    torch.cuda.synchronize()
+    for buf, n in ((ybuf, S * C), (dxbuf, S * C), (dwbuf, C * 4), (dbbuf, C), (wsbuf, nws)):
+        g = buf.view(torch.uint8)
+        k = (buf.numel() - n) // 2 * buf.element_size()
+        assert bool((g[:k] == 0xA5).all()) and bool((g[-k:] == 0xA5).all())
+    ry, ay = oracle.fwd(wc.x, wc.weight, wc.cu_seqlens, wc.bias)
+    bf16_close(_np(y.view(S, C)), ry, ay, "guarded y")
+
+
+def test_empty_sequence():
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    W = torch.randn(64, 4, device=DEV)
+    b = torch.randn(64, device=DEV)
+    cu = torch.zeros(3, dtype=torch.int32, device=DEV)
+    y = vcd.conv1d_fwd(x, W, cu, b)
+    assert y.shape == (0, 64)
+    dW = torch.ones(64, 4, device=DEV)
+    dB = torch.ones(64, device=DEV)
+    dx, dW, dB = vcd.conv1d_bwd(x, x.clone(), W, cu, b, "bf16", dweight=dW, dbias=dB)
+    torch.cuda.synchronize()
+    assert dx.shape == (0, 64) and not dW.any() and not dB.any()
+
+
+def test_cuda_graph_capture_and_replay():
+    """fwd + bwd (with its dependent reduce launch) captured once and replayed."""
+    w = synth.make("tiny", device=DEV)
+    ws = torch.empty(vcd.conv1d_bwd_workspace_size(w.S, w.C), dtype=torch.uint8, device=DEV)
+    y = torch.empty_like(w.x)
+    dx = torch.empty_like(w.x)
+    dW = torch.empty(w.C, 4, device=DEV)
+    dB = torch.empty(w.C, device=DEV)
+
+    def step():
+        vcd.conv1d_fwd(w.x, w.weight, w.cu_seqlens, w.bias, y=y)
+        vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, "bf16", dx=dx, dweight=dW,
+                       dbias=dB, workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (y, dx, dW, dB)]
+    for t in (y, dx, dW, dB):
+        t.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(ref, (y, dx, dW, dB)):
+        assert torch.equal(a, b)
+
+
+def test_binding_errors():
+    w = synth.custom(64, 16, [64], seed=1).to(DEV)
+    with pytest.raises(vcd.VcdError):
+        vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, None, "bf16",
+                       dbias=torch.empty(16, device=DEV))
+    raw = torch.empty(64 * 16 + 8, dtype=torch.bfloat16, device=DEV)
+    xm = raw[1:1 + 64 * 16].view(64, 16)                 # 2-byte offset
+    xm.copy_(w.x)
+    with pytest.raises(vcd.VcdError, match="misaligned"):
+        vcd.conv1d_fwd(xm, w.weight, w.cu_seqlens, w.bias)
+    with pytest.raises(vcd.VcdError, match="workspace"):
+        vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, "bf16",
+                       workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+
+
+def test_native_library_is_loaded():
+    vcd.load_library()
+    maps = open("/proc/self/maps").read()
+    assert os.path.realpath(vcd.library_path()) in maps
+
+
+def test_report_strict_fractions(capsys):
+    """Prints the strict 1-ulp pass fractions gathered above (informational)."""
+    with capsys.disabled():
+        for k, v in sorted(REPORT.items()):
+            if v < 1.0:
+                print(f"  strict-1ulp {k}: {v:.6f}")

@@ -1,0 +1,48 @@
+// vcd_kernels.h -- argument blocks and launchers of the CUDA kernels; the C ABI
+// (vcd_capi.cu) validates arguments and calls these.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "vcd_plan.h"
+
+namespace vcd {
+
+enum BiasKind { kBiasNone = 0, kBiasF32 = 1, kBiasBF16 = 2 };
+
+struct FwdArgs {
+    const void* x;            // BF16 [S, C]
+    const void* weight;       // [C, 4] FP32 or BF16
+    const void* bias;         // [C] or nullptr
+    const int32_t* cu_seqlens;
+    int64_t num_docs;
+    void* y;                  // BF16 [S, C]
+    int weight_bf16;
+    int bias_kind;            // BiasKind
+    Plan plan;                // make_plan(S, C, kFwdVec)
+};
+
+struct BwdArgs {
+    const void* x;            // BF16 [S, C]
+    const void* dy;           // BF16 [S, C]
+    const void* weight;
+    const void* bias;
+    const int32_t* cu_seqlens;
+    int64_t num_docs;
+    void* dx;                 // BF16 [S, C]
+    float* partials;          // [units][32 * kBwdVec][5] FP32
+    void* dweight;            // [C, 4]
+    void* dbias;              // [C] or nullptr
+    int weight_bf16;
+    int bias_kind;
+    int policy;               // 0: SiLU' at bf16(pre), 1: at the FP32 pre
+    int dweight_bf16;
+    int dbias_bf16;
+    Plan plan;                // make_plan(S, C, kBwdVec)
+};
+
+cudaError_t launch_fwd(const FwdArgs& a, int sm_count, cudaStream_t stream);
+// Main kernel, then the reduce kernel launched programmatically dependent on it.
+cudaError_t launch_bwd(const BwdArgs& a, int sm_count, cudaStream_t stream);
+
+}  // namespace vcd
