@@ -156,9 +156,9 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     recipe = synth.RECIPES[args.config]
-    w = synth.make(args.config, device=dev)
+    w = synth.make(args.config, device=dev, S=args.S)
     S, C = w.S, w.C
-    policy = recipe.policies[0]
+    policy = args.policy or recipe.policies[0]
     nws = vcd.conv1d_bwd_workspace_size(S, C)
     wsp = torch.empty(nws, dtype=torch.uint8, device=dev)
     y = torch.empty_like(w.x)
@@ -210,6 +210,8 @@ def run_ours(args):
         total_ms = float(t.item())
 
     # ---- end to end: pinned host buffers through the public API ----
+    if args.no_e2e:
+        return finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, None, ws, rank)
     hx = w.x.cpu().pin_memory()
     hdy = w.dy.cpu().pin_memory()
     hW = w.weight.cpu().pin_memory()
@@ -251,6 +253,12 @@ def run_ours(args):
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    e2e = (e2e_ms, h2d_bytes, d2h_bytes)
+    return finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws, rank)
+
+
+def finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws, rank):
+    import torch.distributed as dist
 
     fwd_b, bwd_b = compulsory_bytes(S, C, nws)
     step_b = fwd_b + bwd_b
@@ -302,9 +310,10 @@ def run_ours(args):
                      "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(bwd_achieved / peak, 4),
                      "traffic": tr, "algorithmic_bytes": bwd_b},
-        "e2e": {"value": round(ws * step_b / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d_bytes,
-                "d2h_bytes_per_step": d2h_bytes},
+        "e2e": None if e2e is None else {
+            "value": round(ws * step_b / (e2e[0] * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(e2e[0], 3), "h2d_bytes_per_step": e2e[1],
+            "d2h_bytes_per_step": e2e[2]},
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "kernel_sha": sha,
@@ -403,6 +412,11 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=96,
                     help="tokens per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--S", type=int, default=None,
+                    help="scale the workload to S tokens (same recipe); profiling runs only")
+    ap.add_argument("--policy", choices=["bf16", "fp32"], default=None,
+                    help="SiLU' policy (default: the workload's own)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
