@@ -120,6 +120,42 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C,
                void* workspace, size_t workspace_bytes,
                cudaStream_t stream);
 
+/* Size of the fixed device scratch used by conv1d_bwd_noalloc: 8 MiB, enough
+ * for every shape with C <= 419328 (the backward's partial rows take about
+ * 6 MB at most below that). */
+#define VCD_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Backward without a workspace argument and without any allocation. The
+ * pages have no counterpart to this entry point; it exists for callers that
+ * cannot hand the library device memory of its own: code embedded in a host
+ * program whose memory is owned by another allocator it cannot reach from C,
+ * or code that must not call cudaMalloc/cudaFree once it is running (those
+ * calls can stall every stream on the device). It computes exactly what
+ * conv1d_bwd computes, with the same arguments minus workspace and
+ * workspace_bytes, and keeps the per-unit partial rows in a fixed
+ * VCD_NOALLOC_SCRATCH_BYTES array compiled into the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   - Shapes whose partial rows exceed VCD_NOALLOC_SCRATCH_BYTES are refused
+ *     with VCD_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - The first call on a device (with S > 0) looks up the array's device
+ *     address on that device (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call shares the one array. It needs no clearing (each call writes
+ *     all the rows it reads), but two calls whose kernels may overlap on the
+ *     GPU -- different streams, no ordering between them -- race on it and
+ *     give wrong gradients; order such calls or use conv1d_bwd with separate
+ *     workspaces.
+ *   - Calls no allocating function (no cudaMalloc, cudaFree or library
+ *     allocator). Other arguments and errors as in conv1d_bwd. */
+int conv1d_bwd_noalloc(const void* x, const void* dy, int64_t S, int64_t C,
+                       const void* weight, int weight_dtype,
+                       const int32_t* cu_seqlens, int64_t num_docs,
+                       const void* bias, int bias_dtype,
+                       int policy,
+                       void* dx, void* dweight, int dweight_dtype,
+                       void* dbias, int dbias_dtype,
+                       cudaStream_t stream);
+
 /* Static description of a vcd_status code (never NULL). */
 const char* conv1d_status_string(int status);
 

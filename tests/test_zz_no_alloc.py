@@ -1,0 +1,72 @@
+"""conv1d_bwd_noalloc -- the backward for callers that cannot give the library
+device memory -- must give what conv1d_bwd gives.
+
+Some callers cannot hand the library a workspace: a plugin inside a host
+program whose device memory belongs to an allocator it cannot reach, or code
+that must not call cudaMalloc/cudaFree while it runs. This entry point keeps its
+partial rows in a fixed array inside the library. The test calls it through the
+C ABI twice in a row (the second call finds the first call's rows in the shared
+array) and compares each result with conv1d_bwd's under the same tolerances as
+the parity tests; both run the same fixed-order reduction, so the bits match.
+
+Named so that pytest collects it last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import varlen_causal_depthwise_gb300 as vcd
+from varlen_causal_depthwise_gb300 import binding, synth
+from _check import REL_L2, bf16_close, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _abi_noalloc(w, policy, dx, dW, dB):
+    lib = vcd.load_library()
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    dt = lambda t: binding.VCD_FP32 if t is None or t.dtype == torch.float32 else binding.VCD_BF16
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return lib.conv1d_bwd_noalloc(p(w.x), p(w.dy), w.S, w.C, p(w.weight), dt(w.weight),
+                                  p(w.cu_seqlens), w.cu_seqlens.numel() - 1, p(w.bias),
+                                  dt(w.bias), binding.POLICIES[policy], p(dx), p(dW), dt(dW),
+                                  p(dB), dt(dB), stream)
+
+
+@pytest.mark.parametrize("name,S,C", [("linattn", 8192, 6144), ("boundary", 4096, 1032),
+                                      ("mid", 3000, 264)])
+def test_noalloc_matches_workspace_entry_point(name, S, C):
+    w = synth.make(name, device=DEV, S=S, C=C)
+    for policy in synth.RECIPES[name].policies:
+        dB_ref = None if w.bias is None else torch.empty(C, device=DEV)
+        ref = vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, policy,
+                             dweight=torch.empty(C, 4, device=DEV), dbias=dB_ref)
+        torch.cuda.synchronize()
+        for call in range(2):
+            dx = torch.full_like(w.x, float("nan"))
+            dW = torch.full((C, 4), float("nan"), device=DEV)
+            dB = None if w.bias is None else torch.full((C,), float("nan"), device=DEV)
+            assert _abi_noalloc(w, policy, dx, dW, dB) == binding.VCD_OK
+            torch.cuda.synchronize()
+            what = f"{name} {policy} call {call}"
+            bf16_close(dx.double().cpu().numpy(), ref[0].double().cpu().numpy(), None, what)
+            assert rel_l2(dW.double().cpu().numpy(), ref[1].double().cpu().numpy()) <= REL_L2[policy]
+            assert torch.equal(dx, ref[0]) and torch.equal(dW, ref[1])
+            if dB is not None:
+                assert rel_l2(dB.double().cpu().numpy(), ref[2].double().cpu().numpy()) <= REL_L2[policy]
+                assert torch.equal(dB, ref[2])
+
+
+def test_noalloc_refuses_shapes_beyond_its_scratch():
+    S, C = 4, 524288          # 4096 channel columns -> 10 MiB of partial rows > 8 MiB
+    assert vcd.conv1d_bwd_workspace_size(S, C) > 8 << 20
+    w = synth.custom(S, C, [S], seed=0).to(DEV)
+    dx = torch.empty_like(w.x)
+    dW = torch.empty(C, 4, device=DEV)
+    dB = torch.empty(C, device=DEV)
+    assert _abi_noalloc(w, "bf16", dx, dW, dB) == binding.VCD_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(vcd.VcdError, match="workspace"):
+        vcd.conv1d_bwd_noalloc(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, "bf16")

@@ -33,6 +33,8 @@ SIGNATURES = {
                           _vp]),
     "conv1d_bwd": (_int, [_vp, _vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _int, _vp,
                           _vp, _int, _vp, _int, _vp, _sz, _vp]),
+    "conv1d_bwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _int,
+                                  _vp, _vp, _int, _vp, _int, _vp]),
     "conv1d_status_string": (ctypes.c_char_p, [_int]),
 }
 
@@ -158,4 +160,31 @@ def conv1d_bwd(x, dy, weight, cu_seqlens, bias=None, policy="bf16", dx=None, dwe
                         _ptr(dx), _ptr(dweight), _dt(dweight), _ptr(dbias), _dt(dbias),
                         _ptr(workspace), nbytes, _stream(stream))
     _check(st, "conv1d_bwd")
+    return dx, dweight, dbias
+
+
+def conv1d_bwd_noalloc(x, dy, weight, cu_seqlens, bias=None, policy="bf16", dx=None,
+                       dweight=None, dbias=None, stream=None, want_dbias=None):
+    """conv1d_bwd for callers that cannot give the library device memory: the
+    partial rows live in the library's fixed scratch array (see include/vcd.h).
+    Outputs not passed in are allocated here by torch, as in conv1d_bwd; the
+    library call itself allocates nothing."""
+    lib = load_library()
+    S, C = _sc(x)
+    if policy not in POLICIES:
+        raise ValueError(f"policy must be 'bf16' or 'fp32', got {policy!r}")
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dweight is None:
+        dweight = torch.empty(C, 4, dtype=weight.dtype, device=x.device)
+    if want_dbias is None:
+        want_dbias = bias is not None
+    if dbias is None and want_dbias:
+        dbias = torch.empty(C, dtype=bias.dtype if bias is not None else torch.float32,
+                            device=x.device)
+    st = lib.conv1d_bwd_noalloc(_ptr(x), _ptr(dy), S, C, _ptr(weight), _dt(weight),
+                                _ptr(cu_seqlens), cu_seqlens.numel() - 1, _ptr(bias), _dt(bias),
+                                POLICIES[policy], _ptr(dx), _ptr(dweight), _dt(dweight),
+                                _ptr(dbias), _dt(dbias), _stream(stream))
+    _check(st, "conv1d_bwd_noalloc")
     return dx, dweight, dbias
