@@ -10,15 +10,19 @@
 //   dw[k]    sum_t dpre[t] x[t - 3 + k]  (zero history)
 //   db       sum_t dpre[t]
 //
-// Main kernel: one warp per work unit (32 groups of 4 channels x L tokens,
-// vcd_plan.h), walking its tokens forward once. The x window (three previous
-// tokens, cleared at a document start) gives pre and the dweight products; dx
-// is produced three tokens late: each new dpre[u] is scattered into the three
-// pending dx accumulators of tokens u-1, u-2, u-3 unless a document start lies
-// between, and dx[u-3] is then complete. The unit reads x over [begin-3,
-// end+3) and dy over [begin, end+3), writes dx over [begin, end), and keeps
-// dweight / dbias in registers; at its end each lane writes its channels' five
-// FP32 sums into the unit's partial row. HBM traffic: 6 bytes per element.
+// Main kernel: one warp per work unit (128 channels x L tokens, vcd_plan.h),
+// walking its tokens forward once. x and dy stream through a per-warp
+// shared-memory ring (cp.async, one batch of kBwdU tokens ahead). Registers
+// hold the x of the three previous tokens and their dpre, so each token gives
+// pre, dpre, its dweight / dbias products, and dx of the token three back in
+// gather form: dx[t-3] = w3 dpre[t-3] + w2 dpre[t-2] + w1 dpre[t-1] + w0 dpre[t].
+// A batch without a document start in positions q-2 .. q+U-1 (one bit mask
+// per batch from cu_seqlens) takes a mask-free path; otherwise each term is
+// predicated on "no document start in between". The unit reads x over
+// [begin-3, end+3) and dy over [begin, end+3), writes dx over [begin, end),
+// and keeps dweight / dbias in registers; at its end each lane writes its
+// channels' five FP32 sums into the unit's partial row. HBM traffic: 6 bytes
+// per element.
 //
 // Reduce kernel: launched with programmatic stream serialization, it waits on
 // griddepcontrol for the main kernel and sums the partial rows of each channel
@@ -35,21 +39,34 @@ namespace vcd {
 namespace {
 
 #ifndef VCD_BWD_U
-#define VCD_BWD_U 4
+#define VCD_BWD_U 8
 #endif
-constexpr int kBwdU = VCD_BWD_U;        // tokens per batch (loads run one batch ahead)
-constexpr int kBP = kBwdVec / 2;        // channel pairs per lane
-constexpr int kFoldBatches = 8;         // "fp32" policy: fold partial sums every 8 batches
-constexpr int kColChannels = 32 * kBwdVec;
+#ifndef VCD_BWD_NS
+#define VCD_BWD_NS 3
+#endif
+#ifndef VCD_BWD_PACKED
+#define VCD_BWD_PACKED 0
+#endif
+constexpr bool kPK = VCD_BWD_PACKED != 0;                 // packed FP32x2 arithmetic
+constexpr int kBwdU = VCD_BWD_U;                          // tokens per batch (even, <= 30)
+constexpr int kBwdNs = VCD_BWD_NS;                        // ring stages (>= 2)
+constexpr int kBwdTensorBytes = kBwdU * kRowBytes;        // one tensor's rows of one stage
+constexpr int kBwdStageBytes = 2 * kBwdTensorBytes;       // x rows, then dy rows
+constexpr int kBwdWarpBytes = kBwdNs * kBwdStageBytes;
+constexpr int kBwdSmemBytes = kWarpsPerCta * kBwdWarpBytes;
+constexpr int kFoldBatches = 32 / kBwdU > 0 ? 32 / kBwdU : 1;   // "fp32": fold every ~32 tokens
+static_assert(kBwdU % 2 == 0 && kBwdU <= 30 && kBwdNs >= 2, "batch geometry");
 
 constexpr int kPolicyBF16 = 0;
 constexpr int kPolicyFP32 = 1;
+
+__device__ __forceinline__ bool bit(uint32_t m, int i) { return (m >> i) & 1u; }
 
 // Neumaier-compensated running sum of float2 values (the "fp32" policy's
 // outer accumulation level).
 struct CompSum2 {
     float2 s, c;
-    __device__ __forceinline__ void zero() { s = c = make_float2(0.f, 0.f); }
+    __device__ __forceinline__ void zero() { s = c = zero2(); }
     __device__ __forceinline__ static void add1(float& s, float& c, float v) {
         const float t = s + v;
         c += fabsf(s) >= fabsf(v) ? (s - t) + v : (v - t) + s;
@@ -59,273 +76,224 @@ struct CompSum2 {
         add1(s.x, c.x, v.x);
         add1(s.y, c.y, v.y);
     }
-    __device__ __forceinline__ float2 get() const { return add2(s, c); }
+    __device__ __forceinline__ float2 get() const { return add2<false>(s, c); }
 };
 
-template <bool W_BF16, int BIAS, int POLICY>
-struct BwdLane {
-    float2 w[4][kBP];
-    float2 b[kBP];
-    float2 xw[3][kBP];   // x[u-3], x[u-2], x[u-1], zero before the document start
-    float2 pd[3][kBP];   // pending dx of tokens u-1, u-2, u-3
-    uint32_t live;       // bit i: pd[i] still receives contributions
-    float2 dw[4][kBP];   // dweight partial sums (inner level under "fp32")
-    float2 db[kBP];
-    CompSum2 odw[4][kBP];   // outer level, "fp32" policy only (unused otherwise)
-    CompSum2 odb[kBP];
-
-    __device__ __forceinline__ void load_params(const BwdArgs& a, int64_t g, bool active) {
-#pragma unroll
-        for (int q = 0; q < kBP; ++q) {
-            b[q] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) w[k][q] = make_float2(0.f, 0.f);
-        }
-        if (!active) return;
-        const int64_t c0 = g * kBwdVec;
-#pragma unroll
-        for (int q = 0; q < kBP; ++q) {
-            if (W_BF16) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                    reinterpret_cast<const __nv_bfloat16*>(a.weight) + (c0 + 2 * q) * 4));
-                const float2 e01 = bf16x2_to_float2(v.x), e23 = bf16x2_to_float2(v.y);
-                const float2 o01 = bf16x2_to_float2(v.z), o23 = bf16x2_to_float2(v.w);
-                w[0][q] = make_float2(e01.x, o01.x);
-                w[1][q] = make_float2(e01.y, o01.y);
-                w[2][q] = make_float2(e23.x, o23.x);
-                w[3][q] = make_float2(e23.y, o23.y);
-            } else {
-                const float4* wp = reinterpret_cast<const float4*>(a.weight) + c0 + 2 * q;
-                const float4 e = __ldg(wp), o = __ldg(wp + 1);
-                w[0][q] = make_float2(e.x, o.x);
-                w[1][q] = make_float2(e.y, o.y);
-                w[2][q] = make_float2(e.z, o.z);
-                w[3][q] = make_float2(e.w, o.w);
-            }
-            if (BIAS == kBiasF32)
-                b[q] = __ldg(reinterpret_cast<const float2*>(a.bias) + c0 / 2 + q);
-            else if (BIAS == kBiasBF16)
-                b[q] = bf16x2_to_float2(__ldg(reinterpret_cast<const uint32_t*>(a.bias) + c0 / 2 + q));
-        }
-    }
-
-    __device__ __forceinline__ void reset() {
-        live = 0;
-#pragma unroll
-        for (int q = 0; q < kBP; ++q) {
-#pragma unroll
-            for (int k = 0; k < 3; ++k) xw[k][q] = pd[k][q] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) dw[k][q] = make_float2(0.f, 0.f);
-            db[q] = make_float2(0.f, 0.f);
-            if (POLICY == kPolicyFP32) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) odw[k][q].zero();
-                odb[q].zero();
-            }
-        }
-    }
-
-    // "fp32" policy: move the inner sums into the compensated outer sums.
-    __device__ __forceinline__ void fold() {
-        if (POLICY != kPolicyFP32) return;
-#pragma unroll
-        for (int q = 0; q < kBP; ++q) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                odw[k][q].add(dw[k][q]);
-                dw[k][q] = make_float2(0.f, 0.f);
-            }
-            odb[q].add(db[q]);
-            db[q] = make_float2(0.f, 0.f);
-        }
-    }
-
-    __device__ __forceinline__ void doc_start() {
-#pragma unroll
-        for (int k = 0; k < 3; ++k)
-#pragma unroll
-            for (int q = 0; q < kBP; ++q) xw[k][q] = make_float2(0.f, 0.f);
-        live = 0;
-    }
-
-    // Warm-up token (before the unit's range): only slides the x window.
-    __device__ __forceinline__ void halo(uint2 xv) {
-#pragma unroll
-        for (int q = 0; q < kBP; ++q) {
-            xw[0][q] = xw[1][q];
-            xw[1][q] = xw[2][q];
-            xw[2][q] = bf16x2_to_float2(q == 0 ? xv.x : xv.y);
-        }
-    }
-
-    // Token u inside [begin, end + 3): dpre, dweight / dbias (if ACC), the
-    // scatter into pending dx, and dx[u - 3] as packed BF16.
-    template <bool ACC, bool ALL_LIVE>
-    __device__ __forceinline__ uint2 token(uint2 xv, uint2 gv) {
-        uint32_t out[kBP];
-#pragma unroll
-        for (int q = 0; q < kBP; ++q) {
-            const float2 xf = bf16x2_to_float2(q == 0 ? xv.x : xv.y);
-            const float2 gf = bf16x2_to_float2(q == 0 ? gv.x : gv.y);
-            float2 pre = fma2(w[0][q], xw[0][q], b[q]);
-            pre = fma2(w[1][q], xw[1][q], pre);
-            pre = fma2(w[2][q], xw[2][q], pre);
-            pre = fma2(w[3][q], xf, pre);
-            float2 sg;
-            if (POLICY == kPolicyBF16) sg = silu_grad2(round_bf16x2(pre));
-            else sg = silu_grad2_precise(pre);
-            const float2 d = mul2(gf, sg);
-            if (ACC) {
-                dw[0][q] = fma2(d, xw[0][q], dw[0][q]);
-                dw[1][q] = fma2(d, xw[1][q], dw[1][q]);
-                dw[2][q] = fma2(d, xw[2][q], dw[2][q]);
-                dw[3][q] = fma2(d, xf, dw[3][q]);
-                if (BIAS != kBiasNone) db[q] = add2(db[q], d);
-            }
-            if (ALL_LIVE || (live & 1u)) pd[0][q] = fma2(w[2][q], d, pd[0][q]);
-            if (ALL_LIVE || (live & 2u)) pd[1][q] = fma2(w[1][q], d, pd[1][q]);
-            if (ALL_LIVE || (live & 4u)) pd[2][q] = fma2(w[0][q], d, pd[2][q]);
-            out[q] = float2_to_bf16x2(pd[2][q]);
-            pd[2][q] = pd[1][q];
-            pd[1][q] = pd[0][q];
-            pd[0][q] = mul2(w[3][q], d);
-            xw[0][q] = xw[1][q];
-            xw[1][q] = xw[2][q];
-            xw[2][q] = xf;
-        }
-        live = ((live << 1) | 1u) & 7u;
-        return make_uint2(out[0], out[1]);
-    }
-
-    // Final sums of channel pair q, element e (0: .x, 1: .y): dw0..3, db.
-    __device__ __forceinline__ void result(int q, float (&r)[2][5]) const {
-        float2 v[5];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            v[k] = POLICY == kPolicyFP32 ? odw[k][q].get() : dw[k][q];
-        v[4] = POLICY == kPolicyFP32 ? odb[q].get() : db[q];
-#pragma unroll
-        for (int k = 0; k < 5; ++k) {
-            r[0][k] = v[k].x;
-            r[1][k] = v[k].y;
-        }
-    }
-};
-
-__device__ __forceinline__ void st_stream2(uint2* p, uint2 v) { __stcs(p, v); }
+template <int POLICY>
+__device__ __forceinline__ float2 grad_at(float2 pre) {
+    if (POLICY == kPolicyBF16) return silu_grad2<kPK>(round_bf16x2(pre));
+    return silu_grad2_precise(pre);
+}
 
 template <bool W_BF16, int BIAS, int POLICY>
-__global__ void __launch_bounds__(kThreadsPerCta, 2) bwd_main_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel(const BwdArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
-    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const Plan& P = a.plan;
-    const int64_t vrow = P.C / kBwdVec;
-    const uint2* __restrict__ x = reinterpret_cast<const uint2*>(a.x);
-    const uint2* __restrict__ dy = reinterpret_cast<const uint2*>(a.dy);
-    uint2* __restrict__ dx = reinterpret_cast<uint2*>(a.dx);
+    const int wid = threadIdx.x >> 5;
+    unsigned char* const ring = smem + wid * kBwdWarpBytes;
+    const uint32_t ring_s = smem_u32(ring);
+    const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + wid;
+    const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+    const int64_t S = a.plan.S, C = a.plan.C, L = a.plan.L;
+    const int64_t units = a.plan.units, ncols = a.plan.ncols;
+    const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(a.x);
+    const __nv_bfloat16* __restrict__ dy = static_cast<const __nv_bfloat16*>(a.dy);
+    __nv_bfloat16* __restrict__ dx = static_cast<__nv_bfloat16*>(a.dx);
+    const int32_t* __restrict__ cu = a.cu_seqlens;
     const int64_t ncu = a.num_docs + 1;
 
-    for (int64_t u = warp0; u < P.units; u += nwarps) {
-        const int64_t col = u % P.ncols, row = u / P.ncols;
-        const int64_t g = col * 32 + lane;
-        const bool active = g < P.groups;
-        const int64_t t_begin = row * P.L;
-        const int64_t t_end = t_begin + P.L < P.S ? t_begin + P.L : P.S;
-        const int64_t u_end = t_end + 3 < P.S ? t_end + 3 : P.S;
+    for (int64_t u = warp0; u < units; u += nwarps) {
+        const int64_t col = u % ncols, row = u / ncols;
+        const int64_t c0 = col * kColChannels + lane * kVec;
+        const bool active = c0 < C;
+        const int64_t t_begin = row * L;
+        const int64_t t_end = t_begin + L < S ? t_begin + L : S;
+        const int64_t u_end = t_end + 3 < S ? t_end + 3 : S;     // dpre needed below u_end
+        const int64_t q0 = t_begin - 3;                          // 3 warm-up tokens
+        // relative token indices (token q0 + r): outputs and dweight for r in
+        // [3, r_end), dpre for r in [3, r_du), batches while r - 3 < r_end
+        const int r_end = (int)(t_end - q0);
+        const int r_du = (int)(u_end - q0);
+        const int nb = (r_end + 3 + kBwdU - 1) / kBwdU;
 
-        BwdLane<W_BF16, BIAS, POLICY> st;
-        st.load_params(a, g, active);
-        st.reset();
+        float2 w[4][2], b[2];
+        load_taps<W_BF16, BIAS>(a.weight, a.bias, c0, active, w, b);
+        int64_t ci = lower_bound_warp(cu, ncu, q0 - 2, lane);
+        uint32_t carry = doc_starts(cu, ncu, ci, q0 - 2, 2, lane);   // bits of q0-2, q0-1
 
-        int64_t p = t_begin >= 3 ? t_begin - 3 : 0;
-        int64_t ci = lower_bound_warp(a.cu_seqlens, ncu, p, lane);
-        const uint2* xp = x + g;
-        const uint2* gp = dy + g;
-        uint2* dxp = dx + g;
-
-        uint2 xA[kBwdU], gA[kBwdU], xB[kBwdU], gB[kBwdU];
-        auto load = [&](uint2 (&xb)[kBwdU], uint2 (&gb)[kBwdU], int64_t q) {
+        float2 xc[3][2], dc[3][2];        // x and dpre of tokens q-3, q-2, q-1
+        float2 dw[4][2], db[2];
+        CompSum2 odw[4][2], odb[2];       // "fp32" policy: outer level
 #pragma unroll
-            for (int j = 0; j < kBwdU; ++j) {
-                const int64_t t = q + j;
-                xb[j] = (active && t < u_end) ? ld_stream(xp + t * vrow) : make_uint2(0, 0);
-                gb[j] = (active && t >= t_begin && t < u_end) ? ld_stream(gp + t * vrow)
-                                                              : make_uint2(0, 0);
+        for (int p = 0; p < 2; ++p) {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) xc[k][p] = dc[k][p] = zero2();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                dw[k][p] = zero2();
+                if (POLICY == kPolicyFP32) odw[k][p].zero();
             }
+            db[p] = zero2();
+            if (POLICY == kPolicyFP32) odb[p].zero();
+        }
+
+        RowStream<2> rs;                 // x over [q0, u_end), dy over [t_begin, u_end)
+        {
+            const __nv_bfloat16* const bases[2] = {x, dy};
+            const int64_t lows[2] = {q0 > 0 ? q0 : 0, t_begin};
+            rs.init(bases, C, col, q0, lows, u_end, lane);
+        }
+        __nv_bfloat16* dxp = dx + (q0 - 3) * C + c0;   // dx row of relative token -3
+        const int64_t dstep = C;
+
+        __syncwarp();                    // the previous unit's reads of the ring are done
+        auto issue = [&](int i, int slot) {
+            if (i < nb) {
+                const uint32_t st = ring_s + slot * kBwdStageBytes;
+                const uint32_t d[2] = {st, st + kBwdTensorBytes};
+                rs.stage<kBwdU>(d, i * kBwdU);
+            }
+            cp_async_commit();
         };
-        int nb = 0;
-        auto step = [&](const uint2 (&xb)[kBwdU], const uint2 (&gb)[kBwdU], int64_t q) {
-            const uint32_t starts = doc_starts(a.cu_seqlens, ncu, ci, q, kBwdU, lane);
-            if (starts == 0 && st.live == 7u && q >= t_begin + 3 && q + kBwdU <= t_end) {
-                // Steady state: no document start, every token accumulates and emits.
+#pragma unroll
+        for (int s = 0; s < kBwdNs - 1; ++s) issue(s, s);
+
+        int slot = 0;
+        for (int i = 0; i < nb; ++i) {
+            cp_async_wait<kBwdNs - 2>();
+            __syncwarp();
+            issue(i + kBwdNs - 1, slot == 0 ? kBwdNs - 1 : slot - 1);
+            const int r0 = i * kBwdU;
+            const int64_t q = q0 + r0;
+            const uint32_t nw = doc_starts(cu, ncu, ci, q, kBwdU, lane);
+            const uint32_t M = carry | (nw << 2);            // bit i <-> token q - 2 + i
+            carry = nw >> (kBwdU - 2);
+            const unsigned char* sx = ring + slot * kBwdStageBytes + lane * 8;
+            const unsigned char* sg = sx + kBwdTensorBytes;
+            __nv_bfloat16* dxq = dxp + (int64_t)r0 * dstep;  // dx row of token q - 3
+
+            if (M == 0 && r0 >= 6 && r0 + kBwdU <= r_end) {
+                // every token accumulates and emits dx three tokens back
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
-                    const uint2 o = st.template token<true, true>(xb[j], gb[j]);
-                    if (active) st_stream2(dxp + (q + j - 3) * vrow, o);
+                    const uint2 xv = lds64(sx + j * kRowBytes);
+                    const uint2 gv = lds64(sg + j * kRowBytes);
+                    uint32_t o[2];
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        const float2 xf = bf16x2_to_float2(p == 0 ? xv.x : xv.y);
+                        const float2 gf = bf16x2_to_float2(p == 0 ? gv.x : gv.y);
+                        float2 pre = fma2<kPK>(w[0][p], xc[0][p], b[p]);
+                        pre = fma2<kPK>(w[1][p], xc[1][p], pre);
+                        pre = fma2<kPK>(w[2][p], xc[2][p], pre);
+                        pre = fma2<kPK>(w[3][p], xf, pre);
+                        const float2 d = mul2<kPK>(gf, grad_at<POLICY>(pre));
+                        dw[0][p] = fma2<kPK>(d, xc[0][p], dw[0][p]);
+                        dw[1][p] = fma2<kPK>(d, xc[1][p], dw[1][p]);
+                        dw[2][p] = fma2<kPK>(d, xc[2][p], dw[2][p]);
+                        dw[3][p] = fma2<kPK>(d, xf, dw[3][p]);
+                        if (BIAS != kBiasNone) db[p] = add2<kPK>(db[p], d);
+                        float2 g = mul2<kPK>(w[3][p], dc[0][p]);
+                        g = fma2<kPK>(w[2][p], dc[1][p], g);
+                        g = fma2<kPK>(w[1][p], dc[2][p], g);
+                        g = fma2<kPK>(w[0][p], d, g);
+                        o[p] = float2_to_bf16x2(g);
+                        xc[0][p] = xc[1][p];
+                        xc[1][p] = xc[2][p];
+                        xc[2][p] = xf;
+                        dc[0][p] = dc[1][p];
+                        dc[1][p] = dc[2][p];
+                        dc[2][p] = d;
+                    }
+                    if (active) st_stream(dxq, make_uint2(o[0], o[1]));
+                    dxq += dstep;
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
-                    const int64_t t = q + j;
-                    if (t >= u_end) break;
-                    if (starts & (1u << j)) st.doc_start();
-                    if (t < t_begin) {
-                        st.halo(xb[j]);
-                        continue;
+                    const int r = r0 + j;
+                    const uint2 xv = lds64(sx + j * kRowBytes);
+                    const uint2 gv = lds64(sg + j * kRowBytes);
+                    // tap k of token t sees x[t-3+k] iff no start in (t-3+k, t]
+                    const bool m1 = !bit(M, j + 2);
+                    const bool m2 = m1 && !bit(M, j + 1);
+                    const bool m3 = m2 && !bit(M, j);
+                    // dx[t-3] sees dpre[t-3+i] iff no start in (t-3, t-3+i]
+                    const bool k1 = !bit(M, j);
+                    const bool k2 = k1 && !bit(M, j + 1);
+                    const bool k3 = k2 && !bit(M, j + 2);
+                    const bool has_d = r >= 3 && r < r_du;
+                    const bool acc = r >= 3 && r < r_end;
+                    const bool emit = active && r >= 6 && r - 3 < r_end;
+                    uint32_t o[2];
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        const float2 xf = bf16x2_to_float2(p == 0 ? xv.x : xv.y);
+                        const float2 gf = bf16x2_to_float2(p == 0 ? gv.x : gv.y);
+                        float2 pre = b[p];
+                        if (m3) pre = fma2<kPK>(w[0][p], xc[0][p], pre);
+                        if (m2) pre = fma2<kPK>(w[1][p], xc[1][p], pre);
+                        if (m1) pre = fma2<kPK>(w[2][p], xc[2][p], pre);
+                        pre = fma2<kPK>(w[3][p], xf, pre);
+                        float2 d = zero2();
+                        if (has_d) d = mul2<kPK>(gf, grad_at<POLICY>(pre));
+                        if (acc) {
+                            if (m3) dw[0][p] = fma2<kPK>(d, xc[0][p], dw[0][p]);
+                            if (m2) dw[1][p] = fma2<kPK>(d, xc[1][p], dw[1][p]);
+                            if (m1) dw[2][p] = fma2<kPK>(d, xc[2][p], dw[2][p]);
+                            dw[3][p] = fma2<kPK>(d, xf, dw[3][p]);
+                            if (BIAS != kBiasNone) db[p] = add2<kPK>(db[p], d);
+                        }
+                        float2 g = mul2<kPK>(w[3][p], dc[0][p]);
+                        if (k1) g = fma2<kPK>(w[2][p], dc[1][p], g);
+                        if (k2) g = fma2<kPK>(w[1][p], dc[2][p], g);
+                        if (k3) g = fma2<kPK>(w[0][p], d, g);
+                        o[p] = float2_to_bf16x2(g);
+                        xc[0][p] = xc[1][p];
+                        xc[1][p] = xc[2][p];
+                        xc[2][p] = xf;
+                        dc[0][p] = dc[1][p];
+                        dc[1][p] = dc[2][p];
+                        dc[2][p] = d;
                     }
-                    const uint2 o = t < t_end ? st.template token<true, false>(xb[j], gb[j])
-                                              : st.template token<false, false>(xb[j], gb[j]);
-                    if (active && t - 3 >= t_begin) st_stream2(dxp + (t - 3) * vrow, o);
+                    if (emit) st_stream(dxq, make_uint2(o[0], o[1]));
+                    dxq += dstep;
                 }
             }
-            if (POLICY == kPolicyFP32 && ++nb == kFoldBatches) {
-                st.fold();
-                nb = 0;
+            if (POLICY == kPolicyFP32 && (i % kFoldBatches == kFoldBatches - 1 || i == nb - 1)) {
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        odw[k][p].add(dw[k][p]);
+                        dw[k][p] = zero2();
+                    }
+                    odb[p].add(db[p]);
+                    db[p] = zero2();
+                }
             }
-        };
-
-        load(xA, gA, p);
-        for (;;) {
-            load(xB, gB, p + kBwdU);
-            step(xA, gA, p);
-            p += kBwdU;
-            if (p >= u_end) break;
-            load(xA, gA, p + kBwdU);
-            step(xB, gB, p);
-            p += kBwdU;
-            if (p >= u_end) break;
-        }
-        st.fold();
-
-        // dx of the last (up to) three tokens: pd[2] = dx[u_end - 3],
-        // pd[1] = dx[u_end - 2], pd[0] = dx[u_end - 1].
-#pragma unroll
-        for (int i = 2; i >= 0; --i) {
-            const int64_t t = u_end - 1 - i;
-            if (active && t >= t_begin && t < t_end)
-                st_stream2(dxp + t * vrow, make_uint2(float2_to_bf16x2(st.pd[i][0]),
-                                                      float2_to_bf16x2(st.pd[i][1])));
+            slot = slot + 1 == kBwdNs ? 0 : slot + 1;
         }
 
-        // Partial row of this unit: [32 * kBwdVec channels][5] FP32.
+        // Partial row of this unit: [kColChannels channels][5] FP32.
         if (active) {
-            float r[kBwdVec][5];
+            float r[kVec][kPartialStride];
 #pragma unroll
-            for (int q = 0; q < kBP; ++q) {
-                float rq[2][5];
-                st.result(q, rq);
+            for (int p = 0; p < 2; ++p) {
 #pragma unroll
                 for (int k = 0; k < 5; ++k) {
-                    r[2 * q][k] = rq[0][k];
-                    r[2 * q + 1][k] = rq[1][k];
+                    float2 v;
+                    if (POLICY == kPolicyFP32) v = k < 4 ? odw[k][p].get() : odb[p].get();
+                    else v = k < 4 ? dw[k][p] : db[p];
+                    r[2 * p][k] = v.x;
+                    r[2 * p + 1][k] = v.y;
                 }
             }
-            float4* dst = reinterpret_cast<float4*>(a.partials + (u * kColChannels + lane * kBwdVec) * kPartialStride);
+            float4* dst = reinterpret_cast<float4*>(
+                a.partials + (u * kColChannels + lane * kVec) * kPartialStride);
             const float* flat = &r[0][0];
 #pragma unroll
-            for (int i = 0; i < kBwdVec * kPartialStride / 4; ++i)
+            for (int i = 0; i < kVec * kPartialStride / 4; ++i)
                 dst[i] = make_float4(flat[4 * i], flat[4 * i + 1], flat[4 * i + 2], flat[4 * i + 3]);
         }
     }
@@ -378,21 +346,37 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(const BwdArgs a) {
 // -------------------------------------------------------------- launch ---
 
 template <bool W_BF16, int BIAS, int POLICY>
-cudaError_t launch_main_t(const BwdArgs& a, int grid, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreadsPerCta);
-    cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<W_BF16, BIAS, POLICY>, a);
+int prepare_main_t() {
+    // Once per (instantiation, device): allow the dynamic shared memory and
+    // read the occupancy; both are host-side queries.
+    static int occ[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (occ[dev] > 0) return occ[dev];
+    if (cudaFuncSetAttribute(bwd_main_kernel<W_BF16, BIAS, POLICY>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<W_BF16, BIAS, POLICY>,
+                                                      kThreadsPerCta, kBwdSmemBytes) != cudaSuccess)
+        return 0;
+    occ[dev] = n;
+    return n;
 }
 
 template <bool W_BF16, int BIAS, int POLICY>
-int occupancy_t() {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<W_BF16, BIAS, POLICY>,
-                                                      kThreadsPerCta, 0) != cudaSuccess)
-        return 1;
-    return n > 0 ? n : 1;
+cudaError_t launch_main_t(const BwdArgs& a, int sm_count, cudaStream_t stream) {
+    const int occ = prepare_main_t<W_BF16, BIAS, POLICY>();
+    if (occ <= 0) return cudaErrorInvalidConfiguration;
+    const int64_t ctas_needed = (a.plan.units + kWarpsPerCta - 1) / kWarpsPerCta;
+    const int64_t resident = (int64_t)sm_count * occ;
+    const int64_t grid = ctas_needed < resident ? ctas_needed : resident;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
+    cfg.blockDim = dim3(kThreadsPerCta);
+    cfg.dynamicSmemBytes = kBwdSmemBytes;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<W_BF16, BIAS, POLICY>, a);
 }
 
 template <typename ACC>
@@ -414,23 +398,13 @@ cudaError_t launch_reduce_t(const BwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_bwd(const BwdArgs& a, int sm_count, cudaStream_t stream) {
     typedef cudaError_t (*L)(const BwdArgs&, int, cudaStream_t);
-    typedef int (*O)();
 #define VCD_ROW(WB, POL) {launch_main_t<WB, kBiasNone, POL>, launch_main_t<WB, kBiasF32, POL>, launch_main_t<WB, kBiasBF16, POL>}
-#define VCD_OROW(WB, POL) {occupancy_t<WB, kBiasNone, POL>, occupancy_t<WB, kBiasF32, POL>, occupancy_t<WB, kBiasBF16, POL>}
     static const L launch[2][2][3] = {{VCD_ROW(false, kPolicyBF16), VCD_ROW(false, kPolicyFP32)},
                                       {VCD_ROW(true, kPolicyBF16), VCD_ROW(true, kPolicyFP32)}};
-    static const O occ[2][2][3] = {{VCD_OROW(false, kPolicyBF16), VCD_OROW(false, kPolicyFP32)},
-                                   {VCD_OROW(true, kPolicyBF16), VCD_OROW(true, kPolicyFP32)}};
 #undef VCD_ROW
-#undef VCD_OROW
     const int wi = a.weight_bf16 ? 1 : 0;
     const int pi = a.policy == kPolicyFP32 ? 1 : 0;
-    const int bi = a.bias_kind;
-    const int64_t ctas_needed = (a.plan.units + kWarpsPerCta - 1) / kWarpsPerCta;
-    const int64_t resident = (int64_t)sm_count * occ[wi][pi][bi]();
-    int64_t grid = ctas_needed < resident ? ctas_needed : resident;
-    if (grid < 1) grid = 1;
-    cudaError_t e = launch[wi][pi][bi](a, (int)grid, stream);
+    cudaError_t e = launch[wi][pi][a.bias_kind](a, sm_count, stream);
     if (e != cudaSuccess) return e;
     return pi ? launch_reduce_t<double>(a, stream) : launch_reduce_t<float>(a, stream);
 }

@@ -10,21 +10,20 @@
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 
 // SM count of the current device (cached; a host-side attribute query).
 int sm_count_of_current(int* sms) {
-    static int cache[kMaxDevices] = {0};
+    static int cache[vcd::kMaxDevices] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return VCD_ERR_CUDA;
-    if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0) {
+    if (dev >= 0 && dev < vcd::kMaxDevices && cache[dev] > 0) {
         *sms = cache[dev];
         return VCD_OK;
     }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         return VCD_ERR_CUDA;
-    if (dev >= 0 && dev < kMaxDevices) cache[dev] = n;
+    if (dev >= 0 && dev < vcd::kMaxDevices) cache[dev] = n;
     *sms = n;
     return VCD_OK;
 }
@@ -95,7 +94,7 @@ int conv1d_fwd(const void* x, int64_t S, int64_t C, const void* weight, int weig
     a.y = y;
     a.weight_bf16 = weight_dtype == VCD_BF16;
     a.bias_kind = !bias ? vcd::kBiasNone : bias_dtype == VCD_BF16 ? vcd::kBiasBF16 : vcd::kBiasF32;
-    a.plan = vcd::make_plan(S, C, vcd::kFwdVec);
+    a.plan = vcd::fwd_plan(S, C);
     return cuda_status(vcd::launch_fwd(a, sms, stream));
 }
 
@@ -145,7 +144,7 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* 
     a.policy = policy;
     a.dweight_bf16 = dweight_dtype == VCD_BF16;
     a.dbias_bf16 = dbias_dtype == VCD_BF16;
-    a.plan = vcd::make_plan(S, C, vcd::kBwdVec);
+    a.plan = vcd::bwd_plan(S, C);
     return cuda_status(vcd::launch_bwd(a, sms, stream));
 }
 

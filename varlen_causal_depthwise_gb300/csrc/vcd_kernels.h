@@ -10,6 +10,8 @@ namespace vcd {
 
 enum BiasKind { kBiasNone = 0, kBiasF32 = 1, kBiasBF16 = 2 };
 
+constexpr int kMaxDevices = 64;
+
 struct FwdArgs {
     const void* x;            // BF16 [S, C]
     const void* weight;       // [C, 4] FP32 or BF16
@@ -19,7 +21,7 @@ struct FwdArgs {
     void* y;                  // BF16 [S, C]
     int weight_bf16;
     int bias_kind;            // BiasKind
-    Plan plan;                // make_plan(S, C, kFwdVec)
+    Plan plan;                // fwd_plan(S, C)
 };
 
 struct BwdArgs {
@@ -30,7 +32,7 @@ struct BwdArgs {
     const int32_t* cu_seqlens;
     int64_t num_docs;
     void* dx;                 // BF16 [S, C]
-    float* partials;          // [units][32 * kBwdVec][5] FP32
+    float* partials;          // [units][kColChannels][5] FP32
     void* dweight;            // [C, 4]
     void* dbias;              // [C] or nullptr
     int weight_bf16;
@@ -38,7 +40,7 @@ struct BwdArgs {
     int policy;               // 0: SiLU' at bf16(pre), 1: at the FP32 pre
     int dweight_bf16;
     int dbias_bf16;
-    Plan plan;                // make_plan(S, C, kBwdVec)
+    Plan plan;                // bwd_plan(S, C)
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, int sm_count, cudaStream_t stream);

@@ -13,20 +13,19 @@
 #include <stdint.h>
 
 #include "vcd.h"
+#include "vcd_kernels.h"
 #include "vcd_plan.h"
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 static __device__ __align__(256) unsigned char g_bwd_scratch[VCD_NOALLOC_SCRATCH_BYTES];
 
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+std::atomic<void*> g_scratch_addr[vcd::kMaxDevices];
 
 // Device address of g_bwd_scratch on the current device (looked up once).
 int scratch_address(void** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VCD_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= vcd::kMaxDevices) return VCD_ERR_CUDA;
     void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
     if (p == nullptr) {
         if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr)
