@@ -105,10 +105,10 @@ def test_no_bias_and_mixed_dtypes():
 
 # ------------------------------------------------------ full size, sampled --
 
-def _unit_edges(S, C, target_units):
+def _unit_edges(S, C, vec, target_units):
     """Token positions next to work-unit edges (sample selection only; mirrors
-    the unit map of 4 channels per lane, 32 lanes per column)."""
-    ncols = -(-(C // 4) // 32)
+    the unit map: vec channels per lane, 32 lanes per column)."""
+    ncols = -(-(C // vec) // 32)
     rows = max(1, min(target_units // ncols, -(-S // 64)))
     L = -(-S // rows)
     edges = np.arange(0, S, L)
@@ -121,7 +121,7 @@ def sample_points(w, n_random, rng):
     starts = np.unique(cu[:-1][cu[:-1] < S])
     special = np.concatenate([
         starts[:40], starts[-10:], (starts[:20] + 1), (starts[:20] + 2), (starts[:20] + 3),
-        _unit_edges(S, C, 152 * 24), _unit_edges(S, C, 152 * 16), [0, 1, 2, S - 3, S - 2, S - 1]])
+        _unit_edges(S, C, 4, 152 * 24), _unit_edges(S, C, 4, 152 * 16), [0, 1, 2, S - 3, S - 2, S - 1]])
     special = np.unique(np.clip(special, 0, S - 1))
     ch = np.unique(np.concatenate([[0, 1, 7, 8, C - 8, C - 1, 127, 128, 255, 256],
                                    rng.integers(0, C, 6)]))

@@ -10,7 +10,8 @@
 //   dw[k]    sum_t dpre[t] x[t - 3 + k]  (zero history)
 //   db       sum_t dpre[t]
 //
-// Main kernel: one warp per work unit (128 channels x L tokens, vcd_plan.h),
+// Main kernel: one warp per work unit (32 * kBwdVec channels x L tokens,
+// vcd_plan.h),
 // walking its tokens forward once. x and dy stream through a per-warp
 // shared-memory ring (cp.async, one batch of kBwdU tokens ahead). Registers
 // hold the x of the three previous tokens and their dpre, so each token gives
@@ -39,18 +40,25 @@ namespace vcd {
 namespace {
 
 #ifndef VCD_BWD_U
-#define VCD_BWD_U 8
+#define VCD_BWD_U 12
 #endif
 #ifndef VCD_BWD_NS
-#define VCD_BWD_NS 3
+#define VCD_BWD_NS 2
 #endif
 #ifndef VCD_BWD_PACKED
 #define VCD_BWD_PACKED 0
 #endif
+#ifndef VCD_BWD_PACKED_ACC
+#define VCD_BWD_PACKED_ACC 0
+#endif
 constexpr bool kPK = VCD_BWD_PACKED != 0;                 // packed FP32x2 arithmetic
+constexpr bool kPA = kPK || VCD_BWD_PACKED_ACC != 0;      // ... for dweight / dbias / dx
 constexpr int kBwdU = VCD_BWD_U;                          // tokens per batch (even, <= 30)
 constexpr int kBwdNs = VCD_BWD_NS;                        // ring stages (>= 2)
-constexpr int kBwdTensorBytes = kBwdU * kRowBytes;        // one tensor's rows of one stage
+constexpr int kNP = kBwdVec / 2;                          // channel pairs per lane
+constexpr int kBwdColCh = 32 * kBwdVec;                   // channels per unit column
+constexpr int kBwdRowBytes = 2 * kBwdColCh;               // bytes of a token's row segment
+constexpr int kBwdTensorBytes = kBwdU * kBwdRowBytes;     // one tensor's rows of one stage
 constexpr int kBwdStageBytes = 2 * kBwdTensorBytes;       // x rows, then dy rows
 constexpr int kBwdWarpBytes = kBwdNs * kBwdStageBytes;
 constexpr int kBwdSmemBytes = kWarpsPerCta * kBwdWarpBytes;
@@ -104,7 +112,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
 
     for (int64_t u = warp0; u < units; u += nwarps) {
         const int64_t col = u % ncols, row = u / ncols;
-        const int64_t c0 = col * kColChannels + lane * kVec;
+        const int64_t c0 = col * kBwdColCh + lane * kBwdVec;
         const bool active = c0 < C;
         const int64_t t_begin = row * L;
         const int64_t t_end = t_begin + L < S ? t_begin + L : S;
@@ -116,16 +124,16 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
         const int r_du = (int)(u_end - q0);
         const int nb = (r_end + 3 + kBwdU - 1) / kBwdU;
 
-        float2 w[4][2], b[2];
-        load_taps<W_BF16, BIAS>(a.weight, a.bias, c0, active, w, b);
+        float2 w[4][kNP], b[kNP];
+        load_taps<W_BF16, BIAS, kNP>(a.weight, a.bias, c0, active, w, b);
         int64_t ci = lower_bound_warp(cu, ncu, q0 - 2, lane);
         uint32_t carry = doc_starts(cu, ncu, ci, q0 - 2, 2, lane);   // bits of q0-2, q0-1
 
-        float2 xc[3][2], dc[3][2];        // x and dpre of tokens q-3, q-2, q-1
-        float2 dw[4][2], db[2];
-        CompSum2 odw[4][2], odb[2];       // "fp32" policy: outer level
+        float2 xc[3][kNP], dc[3][kNP];    // x and dpre of tokens q-3, q-2, q-1
+        float2 dw[4][kNP], db[kNP];
+        CompSum2 odw[4][kNP], odb[kNP];   // "fp32" policy: outer level
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
+        for (int p = 0; p < kNP; ++p) {
 #pragma unroll
             for (int k = 0; k < 3; ++k) xc[k][p] = dc[k][p] = zero2();
 #pragma unroll
@@ -137,7 +145,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
             if (POLICY == kPolicyFP32) odb[p].zero();
         }
 
-        RowStream<2> rs;                 // x over [q0, u_end), dy over [t_begin, u_end)
+        RowStream<2, kBwdRowBytes> rs;                 // x over [q0, u_end), dy over [t_begin, u_end)
         {
             const __nv_bfloat16* const bases[2] = {x, dy};
             const int64_t lows[2] = {q0 > 0 ? q0 : 0, t_begin};
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
             const uint32_t nw = doc_starts(cu, ncu, ci, q, kBwdU, lane);
             const uint32_t M = carry | (nw << 2);            // bit i <-> token q - 2 + i
             carry = nw >> (kBwdU - 2);
-            const unsigned char* sx = ring + slot * kBwdStageBytes + lane * 8;
+            const unsigned char* sx = ring + slot * kBwdStageBytes + lane * (2 * kBwdVec);
             const unsigned char* sg = sx + kBwdTensorBytes;
             __nv_bfloat16* dxq = dxp + (int64_t)r0 * dstep;  // dx row of token q - 3
 
@@ -176,27 +184,27 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
                 // every token accumulates and emits dx three tokens back
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
-                    const uint2 xv = lds64(sx + j * kRowBytes);
-                    const uint2 gv = lds64(sg + j * kRowBytes);
-                    uint32_t o[2];
+                    uint32_t xv[kNP], gv[kNP], o[kNP];
+                    lds_pairs<kBwdVec>(sx + j * kBwdRowBytes, xv);
+                    lds_pairs<kBwdVec>(sg + j * kBwdRowBytes, gv);
 #pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        const float2 xf = bf16x2_to_float2(p == 0 ? xv.x : xv.y);
-                        const float2 gf = bf16x2_to_float2(p == 0 ? gv.x : gv.y);
+                    for (int p = 0; p < kNP; ++p) {
+                        const float2 xf = bf16x2_to_float2(xv[p]);
+                        const float2 gf = bf16x2_to_float2(gv[p]);
                         float2 pre = fma2<kPK>(w[0][p], xc[0][p], b[p]);
                         pre = fma2<kPK>(w[1][p], xc[1][p], pre);
                         pre = fma2<kPK>(w[2][p], xc[2][p], pre);
                         pre = fma2<kPK>(w[3][p], xf, pre);
                         const float2 d = mul2<kPK>(gf, grad_at<POLICY>(pre));
-                        dw[0][p] = fma2<kPK>(d, xc[0][p], dw[0][p]);
-                        dw[1][p] = fma2<kPK>(d, xc[1][p], dw[1][p]);
-                        dw[2][p] = fma2<kPK>(d, xc[2][p], dw[2][p]);
-                        dw[3][p] = fma2<kPK>(d, xf, dw[3][p]);
-                        if (BIAS != kBiasNone) db[p] = add2<kPK>(db[p], d);
-                        float2 g = mul2<kPK>(w[3][p], dc[0][p]);
-                        g = fma2<kPK>(w[2][p], dc[1][p], g);
-                        g = fma2<kPK>(w[1][p], dc[2][p], g);
-                        g = fma2<kPK>(w[0][p], d, g);
+                        dw[0][p] = fma2<kPA>(d, xc[0][p], dw[0][p]);
+                        dw[1][p] = fma2<kPA>(d, xc[1][p], dw[1][p]);
+                        dw[2][p] = fma2<kPA>(d, xc[2][p], dw[2][p]);
+                        dw[3][p] = fma2<kPA>(d, xf, dw[3][p]);
+                        if (BIAS != kBiasNone) db[p] = add2<kPA>(db[p], d);
+                        float2 g = mul2<kPA>(w[3][p], dc[0][p]);
+                        g = fma2<kPA>(w[2][p], dc[1][p], g);
+                        g = fma2<kPA>(w[1][p], dc[2][p], g);
+                        g = fma2<kPA>(w[0][p], d, g);
                         o[p] = float2_to_bf16x2(g);
                         xc[0][p] = xc[1][p];
                         xc[1][p] = xc[2][p];
@@ -205,15 +213,16 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
                         dc[1][p] = dc[2][p];
                         dc[2][p] = d;
                     }
-                    if (active) st_stream(dxq, make_uint2(o[0], o[1]));
+                    if (active) st_pairs<kBwdVec>(dxq, o);
                     dxq += dstep;
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
                     const int r = r0 + j;
-                    const uint2 xv = lds64(sx + j * kRowBytes);
-                    const uint2 gv = lds64(sg + j * kRowBytes);
+                    uint32_t xv[kNP], gv[kNP], o[kNP];
+                    lds_pairs<kBwdVec>(sx + j * kBwdRowBytes, xv);
+                    lds_pairs<kBwdVec>(sg + j * kBwdRowBytes, gv);
                     // tap k of token t sees x[t-3+k] iff no start in (t-3+k, t]
                     const bool m1 = !bit(M, j + 2);
                     const bool m2 = m1 && !bit(M, j + 1);
@@ -225,11 +234,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
                     const bool has_d = r >= 3 && r < r_du;
                     const bool acc = r >= 3 && r < r_end;
                     const bool emit = active && r >= 6 && r - 3 < r_end;
-                    uint32_t o[2];
 #pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        const float2 xf = bf16x2_to_float2(p == 0 ? xv.x : xv.y);
-                        const float2 gf = bf16x2_to_float2(p == 0 ? gv.x : gv.y);
+                    for (int p = 0; p < kNP; ++p) {
+                        const float2 xf = bf16x2_to_float2(xv[p]);
+                        const float2 gf = bf16x2_to_float2(gv[p]);
                         float2 pre = b[p];
                         if (m3) pre = fma2<kPK>(w[0][p], xc[0][p], pre);
                         if (m2) pre = fma2<kPK>(w[1][p], xc[1][p], pre);
@@ -238,16 +246,16 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
                         float2 d = zero2();
                         if (has_d) d = mul2<kPK>(gf, grad_at<POLICY>(pre));
                         if (acc) {
-                            if (m3) dw[0][p] = fma2<kPK>(d, xc[0][p], dw[0][p]);
-                            if (m2) dw[1][p] = fma2<kPK>(d, xc[1][p], dw[1][p]);
-                            if (m1) dw[2][p] = fma2<kPK>(d, xc[2][p], dw[2][p]);
-                            dw[3][p] = fma2<kPK>(d, xf, dw[3][p]);
-                            if (BIAS != kBiasNone) db[p] = add2<kPK>(db[p], d);
+                            if (m3) dw[0][p] = fma2<kPA>(d, xc[0][p], dw[0][p]);
+                            if (m2) dw[1][p] = fma2<kPA>(d, xc[1][p], dw[1][p]);
+                            if (m1) dw[2][p] = fma2<kPA>(d, xc[2][p], dw[2][p]);
+                            dw[3][p] = fma2<kPA>(d, xf, dw[3][p]);
+                            if (BIAS != kBiasNone) db[p] = add2<kPA>(db[p], d);
                         }
-                        float2 g = mul2<kPK>(w[3][p], dc[0][p]);
-                        if (k1) g = fma2<kPK>(w[2][p], dc[1][p], g);
-                        if (k2) g = fma2<kPK>(w[1][p], dc[2][p], g);
-                        if (k3) g = fma2<kPK>(w[0][p], d, g);
+                        float2 g = mul2<kPA>(w[3][p], dc[0][p]);
+                        if (k1) g = fma2<kPA>(w[2][p], dc[1][p], g);
+                        if (k2) g = fma2<kPA>(w[1][p], dc[2][p], g);
+                        if (k3) g = fma2<kPA>(w[0][p], d, g);
                         o[p] = float2_to_bf16x2(g);
                         xc[0][p] = xc[1][p];
                         xc[1][p] = xc[2][p];
@@ -256,13 +264,13 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
                         dc[1][p] = dc[2][p];
                         dc[2][p] = d;
                     }
-                    if (emit) st_stream(dxq, make_uint2(o[0], o[1]));
+                    if (emit) st_pairs<kBwdVec>(dxq, o);
                     dxq += dstep;
                 }
             }
             if (POLICY == kPolicyFP32 && (i % kFoldBatches == kFoldBatches - 1 || i == nb - 1)) {
 #pragma unroll
-                for (int p = 0; p < 2; ++p) {
+                for (int p = 0; p < kNP; ++p) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         odw[k][p].add(dw[k][p]);
@@ -275,11 +283,12 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
             slot = slot + 1 == kBwdNs ? 0 : slot + 1;
         }
 
-        // Partial row of this unit: [kColChannels channels][5] FP32.
+        // Partial row of this unit: [kBwdColCh channels][5] FP32; this lane's
+        // kBwdVec channels are 5 * kBwdVec consecutive floats (8-byte aligned).
         if (active) {
-            float r[kVec][kPartialStride];
+            float r[kBwdVec][kPartialStride];
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
+            for (int p = 0; p < kNP; ++p) {
 #pragma unroll
                 for (int k = 0; k < 5; ++k) {
                     float2 v;
@@ -289,12 +298,12 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
                     r[2 * p + 1][k] = v.y;
                 }
             }
-            float4* dst = reinterpret_cast<float4*>(
-                a.partials + (u * kColChannels + lane * kVec) * kPartialStride);
+            float2* dst = reinterpret_cast<float2*>(
+                a.partials + (u * kBwdColCh + lane * kBwdVec) * kPartialStride);
             const float* flat = &r[0][0];
 #pragma unroll
-            for (int i = 0; i < kVec * kPartialStride / 4; ++i)
-                dst[i] = make_float4(flat[4 * i], flat[4 * i + 1], flat[4 * i + 2], flat[4 * i + 3]);
+            for (int i = 0; i < kBwdVec * kPartialStride / 2; ++i)
+                dst[i] = make_float2(flat[2 * i], flat[2 * i + 1]);
         }
     }
     // Let the reduce kernel's CTAs be scheduled; its griddepcontrol.wait still
@@ -326,9 +335,9 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(const BwdArgs a) {
     const int64_t c = idx / kPartialStride;
     const int k = (int)(idx % kPartialStride);
     if (k == 4 && a.dbias == nullptr) return;
-    const int64_t col = c / kColChannels, ci = c % kColChannels;
-    const float* src = a.partials + (col * kColChannels + ci) * kPartialStride + k;
-    const int64_t stride = P.ncols * kColChannels * kPartialStride;
+    const int64_t col = c / kBwdColCh, ci = c % kBwdColCh;
+    const float* src = a.partials + (col * kBwdColCh + ci) * kPartialStride + k;
+    const int64_t stride = P.ncols * kBwdColCh * kPartialStride;
     ACC acc = 0;
     int64_t r = 0;
     for (; r + 8 <= P.rows; r += 8) {

@@ -6,7 +6,7 @@
 // with zero history before each document's first token.
 //
 // One warp per work unit (128 channels x L tokens, vcd_plan.h); a lane owns 4
-// channels. The warp streams its 256-byte row segments into a shared-memory
+// channels (kFwdVec). The warp streams its 256-byte row segments into a shared-memory
 // ring with cp.async, kFwdNs - 1 batches of kFwdU tokens ahead of the
 // arithmetic, so the loads in flight cost no registers. The three previous
 // tokens of x stay in registers as FP32. Document starts come from a warp-wide
@@ -39,7 +39,9 @@ namespace {
 constexpr bool kPK = VCD_FWD_PACKED != 0;              // packed FP32x2 arithmetic
 constexpr int kFwdU = VCD_FWD_U;                       // tokens per batch (even, <= 30)
 constexpr int kFwdNs = VCD_FWD_NS;                     // ring stages (>= 2)
-constexpr int kFwdStageBytes = kFwdU * kRowBytes;
+constexpr int kFwdColCh = 32 * kFwdVec;               // channels per unit column
+constexpr int kFwdRowBytes = 2 * kFwdColCh;            // bytes of a token's row segment
+constexpr int kFwdStageBytes = kFwdU * kFwdRowBytes;
 constexpr int kFwdWarpBytes = kFwdNs * kFwdStageBytes;
 constexpr int kFwdSmemBytes = kWarpsPerCta * kFwdWarpBytes;
 static_assert(kFwdU % 2 == 0 && kFwdU <= 30 && kFwdNs >= 2, "batch geometry");
@@ -64,7 +66,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
 
     for (int64_t u = warp0; u < units; u += nwarps) {
         const int64_t col = u % ncols, row = u / ncols;
-        const int64_t c0 = col * kColChannels + lane * kVec;
+        const int64_t c0 = col * kFwdColCh + lane * kFwdVec;
         const bool active = c0 < C;
         const int64_t t_begin = row * L;
         const int64_t t_end = t_begin + L < S ? t_begin + L : S;
@@ -73,14 +75,14 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
         const int nb = (n_rel + kFwdU - 1) / kFwdU;
 
         float2 w[4][2], b[2];
-        load_taps<W_BF16, BIAS>(a.weight, a.bias, c0, active, w, b);
+        load_taps<W_BF16, BIAS, 2>(a.weight, a.bias, c0, active, w, b);
         int64_t ci = lower_bound_warp(cu, ncu, q0 - 2, lane);
         uint32_t carry = doc_starts(cu, ncu, ci, q0 - 2, 2, lane);   // bits of q0-2, q0-1
         float2 xc[3][2];                                              // x[q-3], x[q-2], x[q-1]
 #pragma unroll
         for (int k = 0; k < 3; ++k) xc[k][0] = xc[k][1] = zero2();
 
-        RowStream<1> rs;
+        RowStream<1, kFwdRowBytes> rs;
         {
             const __nv_bfloat16* const bases[1] = {x};
             const int64_t lows[1] = {q0 > 0 ? q0 : 0};
@@ -117,13 +119,13 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
             const uint32_t nw = doc_starts(cu, ncu, ci, q, kFwdU, lane);
             const uint32_t M = carry | (nw << 2);        // bit i <-> token q - 2 + i
             carry = nw >> (kFwdU - 2);
-            const unsigned char* st = ring + slot * kFwdStageBytes + lane * 8;
+            const unsigned char* st = ring + slot * kFwdStageBytes + lane * (2 * kFwdVec);
             __nv_bfloat16* yq = yp + (int64_t)r0 * ystep;
 
             if (M == 0 && r0 >= 3 && r0 + kFwdU <= n_rel) {
 #pragma unroll
                 for (int j = 0; j < kFwdU; ++j) {
-                    const uint2 xv = lds64(st + j * kRowBytes);
+                    const uint2 xv = lds64(st + j * kFwdRowBytes);
                     const float2 xf[2] = {bf16x2_to_float2(xv.x), bf16x2_to_float2(xv.y)};
                     uint32_t o[2];
 #pragma unroll
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
 #pragma unroll
                 for (int j = 0; j < kFwdU; ++j) {
                     const int r = r0 + j;
-                    const uint2 xv = lds64(st + j * kRowBytes);
+                    const uint2 xv = lds64(st + j * kFwdRowBytes);
                     const float2 xf[2] = {bf16x2_to_float2(xv.x), bf16x2_to_float2(xv.y)};
                     // tap k of token t sees x[t-3+k] iff no document starts in (t-3+k, t]
                     const bool m1 = !bit(M, j + 2);

@@ -1,8 +1,9 @@
 // vcd_plan.h -- how the [S, C] token x channel plane is cut into work units.
 //
-// A lane owns 4 consecutive channels (8 bytes of BF16 per token); a warp owns
-// 32 lanes, i.e. one 256-byte row segment of 128 channels per token; a
-// "column" is those 128 channels, a "row" a run of L consecutive tokens, and a
+// A lane owns VEC consecutive channels (2 * VEC bytes of BF16 per token: 4
+// channels in the forward, 2 in the backward, whose per-lane state is larger);
+// a warp owns 32 lanes, i.e. one row segment of 32 * VEC channels per token; a
+// "column" is those channels, a "row" a run of L consecutive tokens, and a
 // unit is one (row, column) pair, processed by one warp token by token with a
 // 3-token halo on the left (and on the right in the backward).
 //
@@ -19,9 +20,11 @@ namespace vcd {
 
 constexpr int kWarpsPerCta = 8;
 constexpr int kThreadsPerCta = 32 * kWarpsPerCta;
-constexpr int kVec = 4;                       // channels per lane
-constexpr int kColChannels = 32 * kVec;       // channels per unit column
-constexpr int kRowBytes = kColChannels * 2;   // BF16 bytes per token of a column
+#ifndef VCD_BWD_VEC
+#define VCD_BWD_VEC 4
+#endif
+constexpr int kFwdVec = 4;                    // channels per lane, forward
+constexpr int kBwdVec = VCD_BWD_VEC;          // channels per lane, backward
 constexpr int64_t kMinTokensPerUnit = 64;     // keeps the 3-token halo below 5%
 constexpr int kPartialStride = 5;             // dweight[0..3], dbias per channel
 
@@ -39,18 +42,20 @@ constexpr int64_t kBwdTargetUnits = kGb300Sms * kBwdCtasPerSm * kWarpsPerCta;
 
 struct Plan {
     int64_t S, C;
-    int64_t groups;   // C / kVec
+    int64_t col_channels;   // 32 * VEC
+    int64_t groups;   // C / VEC
     int64_t ncols;    // columns of 32 groups (the last may be partial)
     int64_t rows;     // token ranges per column
     int64_t L;        // tokens per range (the last range may be shorter)
     int64_t units;    // ncols * rows
 };
 
-inline Plan make_plan(int64_t S, int64_t C, int64_t target_units) {
+inline Plan make_plan(int64_t S, int64_t C, int vec, int64_t target_units) {
     Plan p;
     p.S = S;
     p.C = C;
-    p.groups = C / kVec;
+    p.col_channels = 32 * vec;
+    p.groups = C / vec;
     p.ncols = (p.groups + 31) / 32;
     int64_t rows = target_units / p.ncols;
     const int64_t cap = (S + kMinTokensPerUnit - 1) / kMinTokensPerUnit;
@@ -62,15 +67,15 @@ inline Plan make_plan(int64_t S, int64_t C, int64_t target_units) {
     return p;
 }
 
-inline Plan fwd_plan(int64_t S, int64_t C) { return make_plan(S, C, kFwdTargetUnits); }
-inline Plan bwd_plan(int64_t S, int64_t C) { return make_plan(S, C, kBwdTargetUnits); }
+inline Plan fwd_plan(int64_t S, int64_t C) { return make_plan(S, C, kFwdVec, kFwdTargetUnits); }
+inline Plan bwd_plan(int64_t S, int64_t C) { return make_plan(S, C, kBwdVec, kBwdTargetUnits); }
 
-// Bytes of the backward's partial rows: one FP32 row of kColChannels channels
+// Bytes of the backward's partial rows: one FP32 row of 32 * kBwdVec channels
 // x 5 values per unit.
 inline uint64_t bwd_workspace_bytes(int64_t S, int64_t C) {
     if (S <= 0) return 0;
     const Plan p = bwd_plan(S, C);
-    return (uint64_t)p.units * kColChannels * kPartialStride * sizeof(float);
+    return (uint64_t)p.units * p.col_channels * kPartialStride * sizeof(float);
 }
 
 }  // namespace vcd
