@@ -108,7 +108,8 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
     const __nv_bfloat16* __restrict__ dy = static_cast<const __nv_bfloat16*>(a.dy);
     __nv_bfloat16* __restrict__ dx = static_cast<__nv_bfloat16*>(a.dx);
     const int32_t* __restrict__ cu = a.cu_seqlens;
-    const int64_t ncu = a.num_docs + 1;
+    const int ncu = (int)(a.num_docs + 1);
+    const int Ci = (int)C;                               // row stride, elements
 
     for (int64_t u = warp0; u < units; u += nwarps) {
         const int64_t col = u % ncols, row = u / ncols;
@@ -126,8 +127,9 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
 
         float2 w[4][kNP], b[kNP];
         load_taps<W_BF16, BIAS, kNP>(a.weight, a.bias, c0, active, w, b);
-        int64_t ci = lower_bound_warp(cu, ncu, q0 - 2, lane);
-        uint32_t carry = doc_starts(cu, ncu, ci, q0 - 2, 2, lane);   // bits of q0-2, q0-1
+        DocCursor doc;
+        doc.init(cu, ncu, (int)q0 - 2, lane);
+        uint32_t carry = doc.starts((int)q0 - 2, 2, lane);            // bits of q0-2, q0-1
 
         float2 xc[3][kNP], dc[3][kNP];    // x and dpre of tokens q-3, q-2, q-1
         float2 dw[4][kNP], db[kNP];
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
             issue(i + kBwdNs - 1, slot == 0 ? kBwdNs - 1 : slot - 1);
             const int r0 = i * kBwdU;
             const int64_t q = q0 + r0;
-            const uint32_t nw = doc_starts(cu, ncu, ci, q, kBwdU, lane);
+            const uint32_t nw = doc.starts((int)q, kBwdU, lane);
             const uint32_t M = carry | (nw << 2);            // bit i <-> token q - 2 + i
             carry = nw >> (kBwdU - 2);
             const unsigned char* sx = ring + slot * kBwdStageBytes + lane * (2 * kBwdVec);
@@ -213,8 +215,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
                         dc[1][p] = dc[2][p];
                         dc[2][p] = d;
                     }
-                    if (active) st_pairs<kBwdVec>(dxq, o);
-                    dxq += dstep;
+                    if (active) st_pairs<kBwdVec>(dxq + j * Ci, o);
                 }
             } else {
 #pragma unroll
@@ -264,8 +265,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
                         dc[1][p] = dc[2][p];
                         dc[2][p] = d;
                     }
-                    if (emit) st_pairs<kBwdVec>(dxq, o);
-                    dxq += dstep;
+                    if (emit) st_pairs<kBwdVec>(dxq + j * Ci, o);
                 }
             }
             if (POLICY == kPolicyFP32 && (i % kFoldBatches == kFoldBatches - 1 || i == nb - 1)) {

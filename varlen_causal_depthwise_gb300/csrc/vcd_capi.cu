@@ -35,7 +35,9 @@ bool dtype_ok(int d) { return d == VCD_BF16 || d == VCD_FP32; }
 // S fits the int32 cu_seqlens, and a non-empty sequence has documents.
 int check_shape(int64_t S, int64_t C, int64_t num_docs) {
     if (S < 0 || C <= 0 || C % 8 != 0 || num_docs < 0) return VCD_ERR_INVALID_ARG;
-    if (S > INT32_MAX || C > (int64_t)1 << 40) return VCD_ERR_INVALID_ARG;
+    // token positions, document indices and per-batch row offsets stay in 32 bits
+    if (S > INT32_MAX - 64 || num_docs > INT32_MAX - 1 || C > ((int64_t)1 << 26))
+        return VCD_ERR_INVALID_ARG;
     if (S > 0 && num_docs == 0) return VCD_ERR_INVALID_ARG;
     return VCD_OK;
 }

@@ -62,7 +62,8 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
     const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(a.x);
     __nv_bfloat16* __restrict__ y = static_cast<__nv_bfloat16*>(a.y);
     const int32_t* __restrict__ cu = a.cu_seqlens;
-    const int64_t ncu = a.num_docs + 1;
+    const int ncu = (int)(a.num_docs + 1);
+    const int Ci = (int)C;                               // row stride, elements
 
     for (int64_t u = warp0; u < units; u += nwarps) {
         const int64_t col = u % ncols, row = u / ncols;
@@ -76,8 +77,9 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
 
         float2 w[4][2], b[2];
         load_taps<W_BF16, BIAS, 2>(a.weight, a.bias, c0, active, w, b);
-        int64_t ci = lower_bound_warp(cu, ncu, q0 - 2, lane);
-        uint32_t carry = doc_starts(cu, ncu, ci, q0 - 2, 2, lane);   // bits of q0-2, q0-1
+        DocCursor doc;
+        doc.init(cu, ncu, (int)q0 - 2, lane);
+        uint32_t carry = doc.starts((int)q0 - 2, 2, lane);            // bits of q0-2, q0-1
         float2 xc[3][2];                                              // x[q-3], x[q-2], x[q-1]
 #pragma unroll
         for (int k = 0; k < 3; ++k) xc[k][0] = xc[k][1] = zero2();
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
             }
             const int r0 = i * kFwdU;                    // relative index of the batch
             const int64_t q = q0 + r0;
-            const uint32_t nw = doc_starts(cu, ncu, ci, q, kFwdU, lane);
+            const uint32_t nw = doc.starts((int)q, kFwdU, lane);
             const uint32_t M = carry | (nw << 2);        // bit i <-> token q - 2 + i
             carry = nw >> (kFwdU - 2);
             const unsigned char* st = ring + slot * kFwdStageBytes + lane * (2 * kFwdVec);
@@ -139,8 +141,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
                         xc[1][p] = xc[2][p];
                         xc[2][p] = xf[p];
                     }
-                    if (active) st_stream(yq, make_uint2(o[0], o[1]));
-                    yq += ystep;
+                    if (active) st_stream(yq + j * Ci, make_uint2(o[0], o[1]));
                 }
             } else {
 #pragma unroll
@@ -165,8 +166,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
                         xc[1][p] = xc[2][p];
                         xc[2][p] = xf[p];
                     }
-                    if (active && r >= 3 && r < n_rel) st_stream(yq, make_uint2(o[0], o[1]));
-                    yq += ystep;
+                    if (active && r >= 3 && r < n_rel) st_stream(yq + j * Ci, make_uint2(o[0], o[1]));
                 }
             }
             slot = slot + 1 == kFwdNs ? 0 : slot + 1;
