@@ -46,8 +46,10 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ncu DRAM traffic (read + write bytes per launch) of the backward main kernel on
 # the default workload, keyed by the SHA-256 of the kernel sources it was taken
-# on; a changed kernel reports traffic null until it is profiled again.
-NCU_TRAFFIC = {}
+# on; a changed kernel reports traffic null until it is profiled again. Taken on
+# the same workload at S = 16384 (a capture small enough for ncu's replay) and
+# scaled by the 4x units of S = 65536 (traffic is proportional to tokens).
+NCU_TRAFFIC = {"4880e9012bda32a6": 4 * 577.0e6}
 KERNEL_SOURCES = ["varlen_causal_depthwise_gb300/csrc/vcd_bwd.cu",
                   "varlen_causal_depthwise_gb300/csrc/vcd_device.cuh",
                   "varlen_causal_depthwise_gb300/csrc/vcd_plan.h"]
@@ -407,7 +409,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="linattn",
                     choices=["tiny", "mid", "linattn", "boundary", "large"])
-    ap.add_argument("--cpu-tokens", type=int, default=1536,
+    ap.add_argument("--cpu-tokens", type=int, default=4096,
                     help="tokens of the workload the CPU-baseline oracle leg processes")
     ap.add_argument("--ref-tokens", type=int, default=96,
                     help="tokens per step of the reference (oracle) arm")
