@@ -10,3 +10,9 @@ from .binding import (  # noqa: F401
     VcdError, conv1d_bwd, conv1d_bwd_noalloc, conv1d_bwd_workspace_size, conv1d_fwd, conv1d_fwd_workspace_size,
     conv1d_status_string, library_path, load_library,
 )
+from .functional import (  # noqa: F401,E402
+    CakeCausalConv1dFunction, cake_causal_conv1d_train_backward,
+    cake_causal_conv1d_train_backward_workspace, cake_causal_conv1d_train_backward_workspace_bytes,
+    cake_causal_conv1d_train_forward, cake_causal_conv1d_train_forward_workspace,
+    cake_causal_conv1d_train_forward_workspace_bytes, causal_conv1d,
+)
