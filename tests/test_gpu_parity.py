@@ -296,3 +296,27 @@ def test_report_strict_fractions(capsys):
         for k, v in sorted(REPORT.items()):
             if v < 1.0:
                 print(f"  strict-1ulp {k}: {v:.6f}")
+
+
+@pytest.mark.parametrize("cu", [[0, 50, 20, 100], [0, 30, 60], [0, -5, 1000000, 100],
+                                [10, 50, 100], [0, 100, 100, 7, 100]])
+def test_malformed_cu_seqlens_is_memory_safe(cu):
+    """Contents of cu_seqlens the host cannot check give unspecified values but
+    no access outside the tensors (guard bands intact, outputs finite)."""
+    S, C = 100, 264
+    w = synth.custom(S, C, [S], seed=4).to(DEV)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    ybuf, y = _guarded(S * C, torch.bfloat16)
+    dxbuf, dx = _guarded(S * C, torch.bfloat16)
+    dwbuf, dW = _guarded(C * 4, torch.float32)
+    dbbuf, dB = _guarded(C, torch.float32)
+    vcd.conv1d_fwd(w.x, w.weight, cu_t, w.bias, y=y.view(S, C))
+    vcd.conv1d_bwd(w.x, w.dy, w.weight, cu_t, w.bias, "fp32", dx=dx.view(S, C),
+                   dweight=dW.view(C, 4), dbias=dB)
+    torch.cuda.synchronize()
+    for buf, n in ((ybuf, S * C), (dxbuf, S * C), (dwbuf, C * 4), (dbbuf, C)):
+        g = buf.view(torch.uint8)
+        k = (buf.numel() - n) // 2 * buf.element_size()
+        assert bool((g[:k] == 0xA5).all()) and bool((g[-k:] == 0xA5).all())
+    for t in (y, dx, dW, dB):
+        assert bool(torch.isfinite(t.float()).all())
