@@ -63,10 +63,11 @@ int conv1d_fwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
 
 /* Bytes of backward workspace for (S, C): the FP32 partial rows of dweight
  * and dbias (backward page, Parameters: workspace). A function of (S, C)
- * alone, the same for every route (bias or not, dtypes, policy) and every
- * device, so one buffer serves every call of that shape. The kernel writes
- * every byte it later reads: the buffer needs no zeroing. Same errors as the
- * forward query. */
+ * alone: the maximum over every route (bias or not, dtypes, policy; the
+ * "fp32" policy cuts shorter work units and needs the most) and the same on
+ * every device, so one buffer serves every call of that shape. The kernel
+ * writes every byte it later reads: the buffer needs no zeroing. Same errors
+ * as the forward query. */
 int conv1d_bwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
 
 /* Forward (forward page, Returns):
@@ -106,7 +107,8 @@ int conv1d_fwd(const void* x, int64_t S, int64_t C,
  *   dx        [S, C] BF16, written (may not alias x or dy).
  *   dweight   [C, 4] of dweight_dtype, written.
  *   dbias     [C] of dbias_dtype or NULL; non-NULL requires bias != NULL.
- *   workspace at least conv1d_bwd_workspace_size(S, C) bytes, 16-byte aligned.
+ *   workspace conv1d_bwd_workspace_size(S, C) bytes serve every route; the
+ *             call itself checks only what its own route needs. 16-byte aligned.
  *   stream    CUDA stream both kernels are enqueued on.
  * S == 0 writes zero dweight (and dbias) with cudaMemsetAsync and launches
  * no kernel. */
@@ -120,9 +122,11 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C,
                void* workspace, size_t workspace_bytes,
                cudaStream_t stream);
 
-/* Size of the fixed device scratch used by conv1d_bwd_noalloc: 8 MiB, enough
- * for every shape with C <= 419328 (the backward's partial rows take about
- * 6 MB at most below that). */
+/* Size of the fixed device scratch used by conv1d_bwd_noalloc: 8 MiB. Under
+ * the "bf16" policy that holds the partial rows of every shape with
+ * C <= 419328 (about 6 MB at most below that); the "fp32" policy uses one row
+ * per 256 tokens of each 128-channel column (2560 bytes each), so it fits
+ * while ceil(S / 256) * ceil(C / 128) <= 3276, e.g. S <= 17408 at C = 6144. */
 #define VCD_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* Backward without a workspace argument and without any allocation. The

@@ -48,8 +48,9 @@ def test_workspace_queries(lib):
     assert vcd.conv1d_bwd_workspace_size(0, 256) == 0
     n = vcd.conv1d_bwd_workspace_size(65536, 6144)
     assert n > 0 and n % 16 == 0
-    # one FP32 row of 128 channels x 5 values per work unit, about one unit per warp
-    assert n <= 2432 * 128 * 5 * 4
+    # one FP32 row of 128 channels x 5 values per work unit; the "fp32" policy
+    # (one unit per 256 tokens of each of the 48 columns) needs the most
+    assert n == 48 * (65536 // 256) * 128 * 5 * 4
     for bad in ((-1, 8), (8, 0), (8, 12)):
         with pytest.raises(vcd.VcdError):
             vcd.conv1d_bwd_workspace_size(*bad)

@@ -27,8 +27,8 @@
 //
 // Reduce kernel: launched with programmatic stream serialization, it waits on
 // griddepcontrol for the main kernel and sums the partial rows of each channel
-// in row order (FP32, or FP64 under the "fp32" policy), so the gradients are
-// bitwise reproducible for a given (S, C) and route.
+// in a fixed order (FP32, or FP64 under the "fp32" policy), so the gradients
+// are bitwise reproducible for a given (S, C) and route.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -62,7 +62,6 @@ constexpr int kBwdTensorBytes = kBwdU * kBwdRowBytes;     // one tensor's rows o
 constexpr int kBwdStageBytes = 2 * kBwdTensorBytes;       // x rows, then dy rows
 constexpr int kBwdWarpBytes = kBwdNs * kBwdStageBytes;
 constexpr int kBwdSmemBytes = kWarpsPerCta * kBwdWarpBytes;
-constexpr int kFoldBatches = 32 / kBwdU > 0 ? 32 / kBwdU : 1;   // "fp32": fold every ~32 tokens
 static_assert(kBwdU % 2 == 0 && kBwdU <= 30 && kBwdNs >= 2, "batch geometry");
 
 constexpr int kPolicyBF16 = 0;
@@ -70,30 +69,16 @@ constexpr int kPolicyFP32 = 1;
 
 __device__ __forceinline__ bool bit(uint32_t m, int i) { return (m >> i) & 1u; }
 
-// Neumaier-compensated running sum of float2 values (the "fp32" policy's
-// outer accumulation level).
-struct CompSum2 {
-    float2 s, c;
-    __device__ __forceinline__ void zero() { s = c = zero2(); }
-    __device__ __forceinline__ static void add1(float& s, float& c, float v) {
-        const float t = s + v;
-        c += fabsf(s) >= fabsf(v) ? (s - t) + v : (v - t) + s;
-        s = t;
-    }
-    __device__ __forceinline__ void add(float2 v) {
-        add1(s.x, c.x, v.x);
-        add1(s.y, c.y, v.y);
-    }
-    __device__ __forceinline__ float2 get() const { return add2<false>(s, c); }
-};
-
 template <int POLICY>
 __device__ __forceinline__ float2 grad_at(float2 pre) {
     if (POLICY == kPolicyBF16) return silu_grad2<kPK>(round_bf16x2(pre));
-    return silu_grad2_precise(pre);
+    return silu_grad2_accurate(pre);
 }
 
-template <bool W_BF16, int BIAS, int POLICY>
+// SEG: a warp's chunk holds several units (the "fp32" policy's short units);
+// without it every chunk is a single unit and the unit-boundary logic compiles
+// away.
+template <bool W_BF16, int BIAS, int POLICY, bool SEG>
 __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel(const BwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
@@ -111,19 +96,36 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
     const int ncu = (int)(a.num_docs + 1);
     const int Ci = (int)C;                               // row stride, elements
 
-    for (int64_t u = warp0; u < units; u += nwarps) {
-        const int64_t col = u % ncols, row = u / ncols;
+    // Assignment. Each column's rows are cut into chunks of `per` consecutive
+    // rows, about one chunk per resident warp, and a warp streams a whole
+    // chunk as one segment: a pipeline restart happens per chunk, not per
+    // unit. Chunks are dealt row-major (consecutive warps take consecutive
+    // columns of the same chunk), so warps running side by side read whole
+    // token rows. Unit (row, col) always owns partial row row * ncols + col,
+    // whichever warp computes it.
+    const int64_t rows = a.plan.rows;
+    const int64_t warps_per_col = nwarps / ncols > 0 ? nwarps / ncols : 1;
+    const int64_t per = (rows + warps_per_col - 1) / warps_per_col;
+    const int64_t nchunks = (rows + per - 1) / per;
+    for (int64_t asg = warp0; asg < ncols * nchunks; asg += nwarps) {
+        const int64_t col = asg % ncols, chunk = asg / ncols;
+        const int64_t row0 = chunk * per;
+        const int64_t row1 = row0 + per < rows ? row0 + per : rows;
         const int64_t c0 = col * kBwdColCh + lane * kBwdVec;
         const bool active = c0 < C;
-        const int64_t t_begin = row * L;
-        const int64_t t_end = t_begin + L < S ? t_begin + L : S;
+        const int64_t t_begin = row0 * L;
+        const int64_t t_end = row1 * L < S ? row1 * L : S;
         const int64_t u_end = t_end + 3 < S ? t_end + 3 : S;     // dpre needed below u_end
         const int64_t q0 = t_begin - 3;                          // 3 warm-up tokens
         // relative token indices (token q0 + r): outputs and dweight for r in
-        // [3, r_end), dpre for r in [3, r_du), batches while r - 3 < r_end
+        // [3, r_end), dpre for r in [3, r_du), batches while r - 3 < r_end;
+        // unit row0 + k starts at r = 3 + k L
         const int r_end = (int)(t_end - q0);
         const int r_du = (int)(u_end - q0);
         const int nb = (r_end + 3 + kBwdU - 1) / kBwdU;
+        const int Li = (int)L;
+        int64_t cur_row = row0;                                   // unit being accumulated
+        int r_next = SEG && row1 - row0 > 1 ? 3 + Li : INT_MAX;   // where the next unit starts
 
         float2 w[4][kNP], b[kNP];
         load_taps<W_BF16, BIAS, kNP>(a.weight, a.bias, c0, active, w, b);
@@ -132,20 +134,46 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
         uint32_t carry = doc.starts((int)q0 - 2, 2, lane);            // bits of q0-2, q0-1
 
         float2 xc[3][kNP], dc[3][kNP];    // x and dpre of tokens q-3, q-2, q-1
-        float2 dw[4][kNP], db[kNP];
-        CompSum2 odw[4][kNP], odb[kNP];   // "fp32" policy: outer level
+        float2 dw[4][kNP], db[kNP];       // this unit's FP32 sums
 #pragma unroll
         for (int p = 0; p < kNP; ++p) {
 #pragma unroll
             for (int k = 0; k < 3; ++k) xc[k][p] = dc[k][p] = zero2();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                dw[k][p] = zero2();
-                if (POLICY == kPolicyFP32) odw[k][p].zero();
-            }
+            for (int k = 0; k < 4; ++k) dw[k][p] = zero2();
             db[p] = zero2();
-            if (POLICY == kPolicyFP32) odb[p].zero();
         }
+
+        // Write the finished unit's partial row ([kBwdColCh channels][5] FP32;
+        // this lane's kBwdVec channels are 5 * kBwdVec consecutive floats) and
+        // start the next unit's sums from zero.
+        auto flush = [&](int64_t unit_row) {
+            if (active) {
+                float r[kBwdVec][kPartialStride];
+#pragma unroll
+                for (int p = 0; p < kNP; ++p) {
+#pragma unroll
+                    for (int k = 0; k < 5; ++k) {
+                        const float2 val = k < 4 ? dw[k][p] : db[p];
+                        r[2 * p][k] = val.x;
+                        r[2 * p + 1][k] = val.y;
+                    }
+                }
+                const int64_t unit = unit_row * ncols + col;
+                float2* dst = reinterpret_cast<float2*>(
+                    a.partials + (unit * kBwdColCh + lane * kBwdVec) * kPartialStride);
+                const float* flat = &r[0][0];
+#pragma unroll
+                for (int i = 0; i < kBwdVec * kPartialStride / 2; ++i)
+                    dst[i] = make_float2(flat[2 * i], flat[2 * i + 1]);
+            }
+#pragma unroll
+            for (int p = 0; p < kNP; ++p) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dw[k][p] = zero2();
+                db[p] = zero2();
+            }
+        };
 
         RowStream<2, kBwdRowBytes> rs;                 // x over [q0, u_end), dy over [t_begin, u_end)
         {
@@ -182,7 +210,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
             const unsigned char* sg = sx + kBwdTensorBytes;
             __nv_bfloat16* dxq = dxp + (int64_t)r0 * dstep;  // dx row of token q - 3
 
-            if (M == 0 && r0 >= 6 && r0 + kBwdU <= r_end) {
+            if (M == 0 && r0 >= 6 && r0 + kBwdU <= r_end && (!SEG || r_next >= r0 + kBwdU)) {
                 // every token accumulates and emits dx three tokens back
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
@@ -221,6 +249,11 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
                     const int r = r0 + j;
+                    if (SEG && r == r_next) {             // token r starts the next unit
+                        flush(cur_row);
+                        ++cur_row;
+                        r_next = cur_row + 1 < row1 ? r_next + Li : INT_MAX;
+                    }
                     uint32_t xv[kNP], gv[kNP], o[kNP];
                     lds_pairs<kBwdVec>(sx + j * kBwdRowBytes, xv);
                     lds_pairs<kBwdVec>(sg + j * kBwdRowBytes, gv);
@@ -268,43 +301,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
                     if (emit) st_pairs<kBwdVec>(dxq + j * Ci, o);
                 }
             }
-            if (POLICY == kPolicyFP32 && (i % kFoldBatches == kFoldBatches - 1 || i == nb - 1)) {
-#pragma unroll
-                for (int p = 0; p < kNP; ++p) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        odw[k][p].add(dw[k][p]);
-                        dw[k][p] = zero2();
-                    }
-                    odb[p].add(db[p]);
-                    db[p] = zero2();
-                }
-            }
             slot = slot + 1 == kBwdNs ? 0 : slot + 1;
         }
 
-        // Partial row of this unit: [kBwdColCh channels][5] FP32; this lane's
-        // kBwdVec channels are 5 * kBwdVec consecutive floats (8-byte aligned).
-        if (active) {
-            float r[kBwdVec][kPartialStride];
-#pragma unroll
-            for (int p = 0; p < kNP; ++p) {
-#pragma unroll
-                for (int k = 0; k < 5; ++k) {
-                    float2 v;
-                    if (POLICY == kPolicyFP32) v = k < 4 ? odw[k][p].get() : odb[p].get();
-                    else v = k < 4 ? dw[k][p] : db[p];
-                    r[2 * p][k] = v.x;
-                    r[2 * p + 1][k] = v.y;
-                }
-            }
-            float2* dst = reinterpret_cast<float2*>(
-                a.partials + (u * kBwdColCh + lane * kBwdVec) * kPartialStride);
-            const float* flat = &r[0][0];
-#pragma unroll
-            for (int i = 0; i < kBwdVec * kPartialStride / 2; ++i)
-                dst[i] = make_float2(flat[2 * i], flat[2 * i + 1]);
-        }
+        flush(cur_row);
     }
     // Let the reduce kernel's CTAs be scheduled; its griddepcontrol.wait still
     // waits for this whole grid to finish and its writes to be visible.
@@ -324,37 +324,54 @@ template <> __device__ __forceinline__ void store_out<double>(void* base, int64_
     else reinterpret_cast<float*>(base)[i] = (float)v;
 }
 
-// One thread per (channel, value): sums the unit rows of the channel's column
-// in row order 0, 1, ..., rows - 1.
+// Reduce: output (channel c, value k) is the sum over the R unit rows of its
+// column. A CTA handles 32 outputs with 8 threads each: thread s sums the
+// fixed row slice [s R / 8, (s + 1) R / 8) in row order, then thread 0 of the
+// output adds the 8 slice sums in slice order. The order depends on R only, so
+// the result is bitwise reproducible per (S, C, route).
+constexpr int kRedOutputs = 32;
+constexpr int kRedSlices = 8;
+
 template <typename ACC>
-__global__ void __launch_bounds__(256) bwd_reduce_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kRedOutputs * kRedSlices) bwd_reduce_kernel(const BwdArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ ACC part[kRedSlices][kRedOutputs];
     const Plan& P = a.plan;
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= P.C * kPartialStride) return;
-    const int64_t c = idx / kPartialStride;
+    const int o = threadIdx.x % kRedOutputs;          // consecutive threads: consecutive outputs
+    const int sl = threadIdx.x / kRedOutputs;
+    const int64_t idx = (int64_t)blockIdx.x * kRedOutputs + o;
+    const bool valid = idx < P.C * kPartialStride;
+    const int64_t c = valid ? idx / kPartialStride : 0;
     const int k = (int)(idx % kPartialStride);
-    if (k == 4 && a.dbias == nullptr) return;
     const int64_t col = c / kBwdColCh, ci = c % kBwdColCh;
     const float* src = a.partials + (col * kBwdColCh + ci) * kPartialStride + k;
     const int64_t stride = P.ncols * kBwdColCh * kPartialStride;
+    const int64_t r0 = P.rows * sl / kRedSlices, r1 = P.rows * (sl + 1) / kRedSlices;
     ACC acc = 0;
-    int64_t r = 0;
-    for (; r + 8 <= P.rows; r += 8) {
-        float v[8];
+    if (valid && !(k == 4 && a.dbias == nullptr)) {
+        int64_t r = r0;
+        for (; r + 4 <= r1; r += 4) {
+            float v[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (r + j) * stride);
+            for (int j = 0; j < 4; ++j) v[j] = __ldcg(src + (r + j) * stride);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc += (ACC)v[j];
+            for (int j = 0; j < 4; ++j) acc += (ACC)v[j];
+        }
+        for (; r < r1; ++r) acc += (ACC)__ldcg(src + r * stride);
     }
-    for (; r < P.rows; ++r) acc += (ACC)__ldcg(src + r * stride);
-    if (k < 4) store_out<ACC>(a.dweight, c * 4 + k, acc, a.dweight_bf16 != 0);
-    else store_out<ACC>(a.dbias, c, acc, a.dbias_bf16 != 0);
+    part[sl][o] = acc;
+    __syncthreads();
+    if (sl != 0 || !valid || (k == 4 && a.dbias == nullptr)) return;
+    ACC total = part[0][o];
+#pragma unroll
+    for (int j = 1; j < kRedSlices; ++j) total += part[j][o];
+    if (k < 4) store_out<ACC>(a.dweight, c * 4 + k, total, a.dweight_bf16 != 0);
+    else store_out<ACC>(a.dbias, c, total, a.dbias_bf16 != 0);
 }
 
 // -------------------------------------------------------------- launch ---
 
-template <bool W_BF16, int BIAS, int POLICY>
+template <bool W_BF16, int BIAS, int POLICY, bool SEG>
 int prepare_main_t() {
     // Once per (instantiation, device): allow the dynamic shared memory and
     // read the occupancy; both are host-side queries.
@@ -362,11 +379,11 @@ int prepare_main_t() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     if (occ[dev] > 0) return occ[dev];
-    if (cudaFuncSetAttribute(bwd_main_kernel<W_BF16, BIAS, POLICY>,
+    if (cudaFuncSetAttribute(bwd_main_kernel<W_BF16, BIAS, POLICY, SEG>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<W_BF16, BIAS, POLICY>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<W_BF16, BIAS, POLICY, SEG>,
                                                       kThreadsPerCta, kBwdSmemBytes) != cudaSuccess)
         return 0;
     occ[dev] = n;
@@ -375,8 +392,10 @@ int prepare_main_t() {
 
 template <bool W_BF16, int BIAS, int POLICY>
 cudaError_t launch_main_t(const BwdArgs& a, int sm_count, cudaStream_t stream) {
-    const int occ = prepare_main_t<W_BF16, BIAS, POLICY>();
-    if (occ <= 0) return cudaErrorInvalidConfiguration;
+    // Occupancy is the same for both forms (same launch bounds and shared memory).
+    const int occ = prepare_main_t<W_BF16, BIAS, POLICY, false>();
+    if (occ <= 0 || prepare_main_t<W_BF16, BIAS, POLICY, true>() <= 0)
+        return cudaErrorInvalidConfiguration;
     const int64_t ctas_needed = (a.plan.units + kWarpsPerCta - 1) / kWarpsPerCta;
     const int64_t resident = (int64_t)sm_count * occ;
     const int64_t grid = ctas_needed < resident ? ctas_needed : resident;
@@ -385,7 +404,12 @@ cudaError_t launch_main_t(const BwdArgs& a, int sm_count, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreadsPerCta);
     cfg.dynamicSmemBytes = kBwdSmemBytes;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<W_BF16, BIAS, POLICY>, a);
+    // the kernel cuts each column into chunks of `per` rows, one per warp
+    const int64_t nwarps = (int64_t)cfg.gridDim.x * kWarpsPerCta;
+    const int64_t wpc = nwarps / a.plan.ncols > 0 ? nwarps / a.plan.ncols : 1;
+    const int64_t per = (a.plan.rows + wpc - 1) / wpc;
+    if (per > 1) return cudaLaunchKernelEx(&cfg, bwd_main_kernel<W_BF16, BIAS, POLICY, true>, a);
+    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<W_BF16, BIAS, POLICY, false>, a);
 }
 
 template <typename ACC>
@@ -395,8 +419,8 @@ cudaError_t launch_reduce_t(const BwdArgs& a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     const int64_t n = a.plan.C * kPartialStride;
-    cfg.gridDim = dim3((unsigned)((n + 255) / 256));
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3((unsigned)((n + kRedOutputs - 1) / kRedOutputs));
+    cfg.blockDim = dim3(kRedOutputs * kRedSlices);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;

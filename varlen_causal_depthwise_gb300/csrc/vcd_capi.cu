@@ -124,7 +124,7 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* 
     if (!dy || !dx) return VCD_ERR_INVALID_ARG;
     if (!aligned(dy, 16) || !aligned(dx, 16)) return VCD_ERR_MISALIGNED;
     if (dx == x || dx == dy) return VCD_ERR_INVALID_ARG;
-    const uint64_t need = vcd::bwd_workspace_bytes(S, C);
+    const uint64_t need = vcd::bwd_workspace_bytes_for(S, C, policy);   // this route's rows
     if (!workspace || workspace_bytes < need) return VCD_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 16)) return VCD_ERR_MISALIGNED;
     int sms = 0;
@@ -146,7 +146,7 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* 
     a.policy = policy;
     a.dweight_bf16 = dweight_dtype == VCD_BF16;
     a.dbias_bf16 = dbias_dtype == VCD_BF16;
-    a.plan = vcd::bwd_plan(S, C);
+    a.plan = vcd::bwd_plan(S, C, policy);
     return cuda_status(vcd::launch_bwd(a, sms, stream));
 }
 

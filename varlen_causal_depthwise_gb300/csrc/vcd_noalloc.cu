@@ -46,7 +46,7 @@ extern "C" int conv1d_bwd_noalloc(const void* x, const void* dy, int64_t S, int6
                                   cudaStream_t stream) {
     void* scratch = nullptr;
     if (S > 0 && C > 0) {
-        if (vcd::bwd_workspace_bytes(S, C) > (uint64_t)VCD_NOALLOC_SCRATCH_BYTES)
+        if (vcd::bwd_workspace_bytes_for(S, C, policy) > (uint64_t)VCD_NOALLOC_SCRATCH_BYTES)
             return VCD_ERR_WORKSPACE_TOO_SMALL;   // shape needs more than the fixed scratch
         const int st = scratch_address(&scratch);
         if (st != VCD_OK) return st;

@@ -68,14 +68,38 @@ inline Plan make_plan(int64_t S, int64_t C, int vec, int64_t target_units) {
 }
 
 inline Plan fwd_plan(int64_t S, int64_t C) { return make_plan(S, C, kFwdVec, kFwdTargetUnits); }
-inline Plan bwd_plan(int64_t S, int64_t C) { return make_plan(S, C, kBwdVec, kBwdTargetUnits); }
 
-// Bytes of the backward's partial rows: one FP32 row of 32 * kBwdVec channels
-// x 5 values per unit.
-inline uint64_t bwd_workspace_bytes(int64_t S, int64_t C) {
+// The "fp32" SiLU' policy keeps each unit's FP32 dweight / dbias sums short
+// (at most kFp32TokensPerUnit tokens, relative rounding error about
+// 0.2 * 2^-24 * sqrt(256) = 2e-7) and leaves the rest of the sum to the FP64
+// reduction over units; the "bf16" policy's 5e-5 tolerance allows long units.
+#ifndef VCD_FP32_UNIT_TOKENS
+#define VCD_FP32_UNIT_TOKENS 256
+#endif
+constexpr int64_t kFp32TokensPerUnit = VCD_FP32_UNIT_TOKENS;
+
+inline Plan bwd_plan(int64_t S, int64_t C, int policy) {
+    Plan p = make_plan(S, C, kBwdVec, kBwdTargetUnits);
+    if (policy == 1 && p.L > kFp32TokensPerUnit && S > 0) {
+        p.L = kFp32TokensPerUnit;
+        p.rows = (S + p.L - 1) / p.L;
+        p.units = p.ncols * p.rows;
+    }
+    return p;
+}
+
+// Bytes of one route's partial rows: one FP32 row of 32 * kBwdVec channels x
+// 5 values per unit.
+inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy) {
     if (S <= 0) return 0;
-    const Plan p = bwd_plan(S, C);
+    const Plan p = bwd_plan(S, C, policy);
     return (uint64_t)p.units * p.col_channels * kPartialStride * sizeof(float);
+}
+
+// The most any route needs (the "fp32" policy's plan has at least as many units).
+inline uint64_t bwd_workspace_bytes(int64_t S, int64_t C) {
+    const uint64_t a = bwd_workspace_bytes_for(S, C, 0), b = bwd_workspace_bytes_for(S, C, 1);
+    return a > b ? a : b;
 }
 
 }  // namespace vcd
