@@ -103,14 +103,15 @@ __global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel
     // columns of the same chunk), so warps running side by side read whole
     // token rows. Unit (row, col) always owns partial row row * ncols + col,
     // whichever warp computes it.
+    // Without SEG every chunk is one unit and the loop is over units.
     const int64_t rows = a.plan.rows;
     const int64_t warps_per_col = nwarps / ncols > 0 ? nwarps / ncols : 1;
-    const int64_t per = (rows + warps_per_col - 1) / warps_per_col;
-    const int64_t nchunks = (rows + per - 1) / per;
-    for (int64_t asg = warp0; asg < ncols * nchunks; asg += nwarps) {
+    const int64_t per = SEG ? (rows + warps_per_col - 1) / warps_per_col : 1;
+    const int64_t n_asg = SEG ? ncols * ((rows + per - 1) / per) : units;
+    for (int64_t asg = warp0; asg < n_asg; asg += nwarps) {
         const int64_t col = asg % ncols, chunk = asg / ncols;
-        const int64_t row0 = chunk * per;
-        const int64_t row1 = row0 + per < rows ? row0 + per : rows;
+        const int64_t row0 = SEG ? chunk * per : chunk;
+        const int64_t row1 = !SEG ? row0 + 1 : row0 + per < rows ? row0 + per : rows;
         const int64_t c0 = col * kBwdColCh + lane * kBwdVec;
         const bool active = c0 < C;
         const int64_t t_begin = row0 * L;
