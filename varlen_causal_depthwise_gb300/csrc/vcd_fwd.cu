@@ -28,15 +28,19 @@ namespace vcd {
 namespace {
 
 #ifndef VCD_FWD_U
-#define VCD_FWD_U 8
+#define VCD_FWD_U 4
 #endif
 #ifndef VCD_FWD_NS
-#define VCD_FWD_NS 3
+#define VCD_FWD_NS 6
 #endif
 #ifndef VCD_FWD_PACKED
 #define VCD_FWD_PACKED 1
 #endif
-constexpr bool kPK = VCD_FWD_PACKED != 0;              // packed FP32x2 arithmetic
+#ifndef VCD_FWD_PACKED_SILU
+#define VCD_FWD_PACKED_SILU 0
+#endif
+constexpr bool kPK = VCD_FWD_PACKED != 0;              // packed FP32x2 arithmetic (taps)
+constexpr bool kPKS = VCD_FWD_PACKED_SILU != 0;        // ... (SiLU)
 constexpr int kFwdU = VCD_FWD_U;                       // tokens per batch (even, <= 30)
 constexpr int kFwdNs = VCD_FWD_NS;                     // ring stages (>= 2)
 constexpr int kFwdColCh = 32 * kFwdVec;               // channels per unit column
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
                         pre = fma2<kPK>(w[1][p], xc[1][p], pre);
                         pre = fma2<kPK>(w[2][p], xc[2][p], pre);
                         pre = fma2<kPK>(w[3][p], xf[p], pre);
-                        o[p] = float2_to_bf16x2(silu2<kPK>(pre));
+                        o[p] = float2_to_bf16x2(silu2<kPKS>(pre));
                         xc[0][p] = xc[1][p];
                         xc[1][p] = xc[2][p];
                         xc[2][p] = xf[p];
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
                         if (m2) pre = fma2<kPK>(w[1][p], xc[1][p], pre);
                         if (m1) pre = fma2<kPK>(w[2][p], xc[2][p], pre);
                         pre = fma2<kPK>(w[3][p], xf[p], pre);
-                        o[p] = float2_to_bf16x2(silu2<kPK>(pre));
+                        o[p] = float2_to_bf16x2(silu2<kPKS>(pre));
                         xc[0][p] = xc[1][p];
                         xc[1][p] = xc[2][p];
                         xc[2][p] = xf[p];
