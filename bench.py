@@ -150,6 +150,12 @@ def reduce_max(value, device):
     return float(t.item())
 
 
+def vcd_route_bytes(S, C, policy):
+    import varlen_causal_depthwise_gb300 as vcd
+
+    return vcd.conv1d_bwd_route_workspace_size(S, C, policy)
+
+
 def compulsory_bytes(S, C, partial_bytes):
     E = S * C
     fwd = 4 * E
@@ -297,7 +303,9 @@ def e2e_pipelined(w, policy, K, dev, vcd):
 def finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws, rank):
     import torch.distributed as dist
 
-    fwd_b, bwd_b = compulsory_bytes(S, C, nws)
+    # the partial rows this route writes and reads back (the size query is the
+    # maximum over routes)
+    fwd_b, bwd_b = compulsory_bytes(S, C, vcd_route_bytes(S, C, policy))
     step_b = fwd_b + bwd_b
     ms_step = total_ms / K
     peak, peak_kind = measured_peak()

@@ -70,6 +70,13 @@ int conv1d_fwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
  * as the forward query. */
 int conv1d_bwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
 
+/* Bytes of backward workspace one route needs: the partial rows of the
+ * "bf16" (policy 0) or "fp32" (policy 1) program for (S, C); at most
+ * conv1d_bwd_workspace_size(S, C). A conv1d_bwd call of that policy accepts
+ * a workspace of this size. Errors as the queries above, plus
+ * VCD_ERR_INVALID_ARG for an unknown policy. */
+int conv1d_bwd_route_workspace_size(int64_t S, int64_t C, int policy, size_t* bytes);
+
 /* Forward (forward page, Returns):
  *   y[t, c] = bf16(silu(sum_k weight[c, k] * x[t - 3 + k, c] + bias[c]))
  * with zero history before each document's first token, FP32 arithmetic,

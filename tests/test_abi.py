@@ -54,6 +54,11 @@ def test_workspace_queries(lib):
     for bad in ((-1, 8), (8, 0), (8, 12)):
         with pytest.raises(vcd.VcdError):
             vcd.conv1d_bwd_workspace_size(*bad)
+    bf, fp = (vcd.conv1d_bwd_route_workspace_size(65536, 6144, p) for p in ("bf16", "fp32"))
+    assert bf < fp == n
+    assert bf == 48 * 50 * 128 * 5 * 4        # one row per warp-sized unit (2400 units)
+    with pytest.raises(ValueError):
+        vcd.conv1d_bwd_route_workspace_size(8, 8, "fp16")
 
 
 def _fwd(lib, **kw):

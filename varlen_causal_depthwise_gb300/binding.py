@@ -29,6 +29,7 @@ _vp, _i64, _int, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_s
 SIGNATURES = {
     "conv1d_fwd_workspace_size": (_int, [_i64, _i64, ctypes.POINTER(_sz)]),
     "conv1d_bwd_workspace_size": (_int, [_i64, _i64, ctypes.POINTER(_sz)]),
+    "conv1d_bwd_route_workspace_size": (_int, [_i64, _i64, _int, ctypes.POINTER(_sz)]),
     "conv1d_fwd": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _vp, _vp, _sz,
                           _vp]),
     "conv1d_bwd": (_int, [_vp, _vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _int, _vp,
@@ -111,6 +112,17 @@ def conv1d_bwd_workspace_size(S, C):
     n = ctypes.c_size_t(0)
     _check(load_library().conv1d_bwd_workspace_size(int(S), int(C), ctypes.byref(n)),
            "conv1d_bwd_workspace_size")
+    return n.value
+
+
+def conv1d_bwd_route_workspace_size(S, C, policy="bf16"):
+    """Bytes one policy's program needs (at most conv1d_bwd_workspace_size)."""
+    if policy not in POLICIES:
+        raise ValueError(f"policy must be 'bf16' or 'fp32', got {policy!r}")
+    n = ctypes.c_size_t(0)
+    _check(load_library().conv1d_bwd_route_workspace_size(int(S), int(C), POLICIES[policy],
+                                                          ctypes.byref(n)),
+           "conv1d_bwd_route_workspace_size")
     return n.value
 
 

@@ -70,6 +70,13 @@ int conv1d_bwd_workspace_size(int64_t S, int64_t C, size_t* bytes) {
     return VCD_OK;
 }
 
+int conv1d_bwd_route_workspace_size(int64_t S, int64_t C, int policy, size_t* bytes) {
+    if (!bytes || check_shape(S, C, S > 0 ? 1 : 0) != VCD_OK) return VCD_ERR_INVALID_ARG;
+    if (policy != VCD_SILU_GRAD_BF16 && policy != VCD_SILU_GRAD_FP32) return VCD_ERR_INVALID_ARG;
+    *bytes = (size_t)vcd::bwd_workspace_bytes_for(S, C, policy);
+    return VCD_OK;
+}
+
 int conv1d_fwd(const void* x, int64_t S, int64_t C, const void* weight, int weight_dtype,
                const int32_t* cu_seqlens, int64_t num_docs, const void* bias, int bias_dtype,
                void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream) {

@@ -76,8 +76,8 @@ def cake_causal_conv1d_train_backward_workspace(S, C, device=None):
                        device=dev)
 
 
-def _bwd_workspace(x, S, C, workspace):
-    need = binding.conv1d_bwd_workspace_size(S, C)
+def _bwd_workspace(x, S, C, workspace, policy):
+    need = binding.conv1d_bwd_route_workspace_size(S, C, policy)
     if workspace is not None:
         if workspace.numel() * workspace.element_size() < need:
             raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} "
@@ -130,7 +130,7 @@ def cake_causal_conv1d_train_backward(x, weight, cu_seqlens, dy, *, bias=None,
         dweight = torch.empty(C, 4, dtype=weight.dtype, device=x.device)
     if bias is not None and dbias is None:
         dbias = torch.empty(C, dtype=bias.dtype, device=x.device)
-    ws = _bwd_workspace(x, S, C, workspace) if S > 0 else workspace
+    ws = _bwd_workspace(x, S, C, workspace, silu_grad_preactivation) if S > 0 else workspace
     binding.conv1d_bwd(x, dy, weight, cu_seqlens, bias=bias, policy=silu_grad_preactivation,
                        dx=dx, dweight=dweight, dbias=dbias, workspace=ws)
     return (dx, dweight) if bias is None else (dx, dweight, dbias)
