@@ -320,3 +320,26 @@ def test_malformed_cu_seqlens_is_memory_safe(cu):
         assert bool((g[:k] == 0xA5).all()) and bool((g[-k:] == 0xA5).all())
     for t in (y, dx, dW, dB):
         assert bool(torch.isfinite(t.float()).all())
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes_documents_dtypes(seed):
+    """Seeded random problems: S up to 3000, C a multiple of 8 up to 1040, random
+    document structures (empty documents, single tokens, long runs), every
+    weight / bias dtype pair, both policies; every element against the oracle."""
+    rng = np.random.default_rng(10_000 + seed)
+    S = int(rng.integers(1, 3000))
+    C = 8 * int(rng.integers(1, 131))
+    kind = seed % 3
+    if kind == 0:
+        lengths = synth.doc_lengths(("uniform", 0, int(rng.integers(1, 40)), int(rng.integers(0, 4))),
+                                    S, rng)
+    elif kind == 1:
+        lengths = synth.doc_lengths(("geometric", float(rng.integers(2, 500))), S, rng)
+    else:
+        lengths = synth.doc_lengths(("lognormal", int(rng.integers(1, 9)), 300.0, 1.5), S, rng)
+    wdt = [torch.float32, torch.bfloat16][int(rng.integers(0, 2))]
+    bdt = [None, torch.float32, torch.bfloat16][int(rng.integers(0, 3))]
+    wc = synth.custom(S, C, lengths, seed=seed, x_sigma=float(rng.choice([0.5, 1.0, 3.0])),
+                      weight_dtype=wdt, bias_dtype=bdt)
+    full_check(wc, ("bf16", "fp32"), f"random seed={seed} S={S} C={C}")

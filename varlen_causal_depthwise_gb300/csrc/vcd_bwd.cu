@@ -61,7 +61,7 @@ constexpr int kBwdRowBytes = 2 * kBwdColCh;               // bytes of a token's 
 constexpr int kBwdTensorBytes = kBwdU * kBwdRowBytes;     // one tensor's rows of one stage
 constexpr int kBwdStageBytes = 2 * kBwdTensorBytes;       // x rows, then dy rows
 constexpr int kBwdWarpBytes = kBwdNs * kBwdStageBytes;
-constexpr int kBwdSmemBytes = kWarpsPerCta * kBwdWarpBytes;
+constexpr int kBwdSmemBytes = kBwdWarpsPerCta * kBwdWarpBytes;
 static_assert(kBwdU % 2 == 0 && kBwdU <= 30 && kBwdNs >= 2, "batch geometry");
 
 constexpr int kPolicyBF16 = 0;
@@ -79,14 +79,14 @@ __device__ __forceinline__ float2 grad_at(float2 pre) {
 // without it every chunk is a single unit and the unit-boundary logic compiles
 // away.
 template <bool W_BF16, int BIAS, int POLICY, bool SEG>
-__global__ void __launch_bounds__(kThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kBwdThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel(const BwdArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
     unsigned char* const ring = smem + wid * kBwdWarpBytes;
     const uint32_t ring_s = smem_u32(ring);
-    const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + wid;
-    const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+    const int64_t warp0 = (int64_t)blockIdx.x * kBwdWarpsPerCta + wid;
+    const int64_t nwarps = (int64_t)gridDim.x * kBwdWarpsPerCta;
     const int64_t S = a.plan.S, C = a.plan.C, L = a.plan.L;
     const int64_t units = a.plan.units, ncols = a.plan.ncols;
     const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(a.x);
@@ -385,7 +385,7 @@ int prepare_main_t() {
         return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<W_BF16, BIAS, POLICY, SEG>,
-                                                      kThreadsPerCta, kBwdSmemBytes) != cudaSuccess)
+                                                      kBwdThreadsPerCta, kBwdSmemBytes) != cudaSuccess)
         return 0;
     occ[dev] = n;
     return n;
@@ -397,16 +397,16 @@ cudaError_t launch_main_t(const BwdArgs& a, int sm_count, cudaStream_t stream) {
     const int occ = prepare_main_t<W_BF16, BIAS, POLICY, false>();
     if (occ <= 0 || prepare_main_t<W_BF16, BIAS, POLICY, true>() <= 0)
         return cudaErrorInvalidConfiguration;
-    const int64_t ctas_needed = (a.plan.units + kWarpsPerCta - 1) / kWarpsPerCta;
+    const int64_t ctas_needed = (a.plan.units + kBwdWarpsPerCta - 1) / kBwdWarpsPerCta;
     const int64_t resident = (int64_t)sm_count * occ;
     const int64_t grid = ctas_needed < resident ? ctas_needed : resident;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
-    cfg.blockDim = dim3(kThreadsPerCta);
+    cfg.blockDim = dim3(kBwdThreadsPerCta);
     cfg.dynamicSmemBytes = kBwdSmemBytes;
     cfg.stream = stream;
     // the kernel cuts each column into chunks of `per` rows, one per warp
-    const int64_t nwarps = (int64_t)cfg.gridDim.x * kWarpsPerCta;
+    const int64_t nwarps = (int64_t)cfg.gridDim.x * kBwdWarpsPerCta;
     const int64_t wpc = nwarps / a.plan.ncols > 0 ? nwarps / a.plan.ncols : 1;
     const int64_t per = (a.plan.rows + wpc - 1) / wpc;
     if (per > 1) return cudaLaunchKernelEx(&cfg, bwd_main_kernel<W_BF16, BIAS, POLICY, true>, a);

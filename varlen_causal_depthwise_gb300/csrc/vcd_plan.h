@@ -38,7 +38,12 @@ constexpr int kFwdCtasPerSm = VCD_FWD_CTAS_PER_SM;
 constexpr int kBwdCtasPerSm = VCD_BWD_CTAS_PER_SM;
 constexpr int64_t kGb300Sms = 152;
 constexpr int64_t kFwdTargetUnits = kGb300Sms * kFwdCtasPerSm * kWarpsPerCta;
-constexpr int64_t kBwdTargetUnits = kGb300Sms * kBwdCtasPerSm * kWarpsPerCta;
+#ifndef VCD_BWD_WARPS_PER_CTA
+#define VCD_BWD_WARPS_PER_CTA 8
+#endif
+constexpr int kBwdWarpsPerCta = VCD_BWD_WARPS_PER_CTA;
+constexpr int kBwdThreadsPerCta = 32 * kBwdWarpsPerCta;
+constexpr int64_t kBwdTargetUnits = kGb300Sms * kBwdCtasPerSm * kBwdWarpsPerCta;
 
 struct Plan {
     int64_t S, C;
