@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import varlen_causal_depthwise_gb300 as vcd
 from varlen_causal_depthwise_gb300 import binding
@@ -126,3 +127,17 @@ def test_binding_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "libvcd.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         binding.load_library()
+
+
+def test_binding_rejects_host_tensors_before_any_call():
+    """The C ABI takes bare device pointers: the binding must refuse host memory
+    itself rather than hand the library a host address."""
+    x = torch.zeros(16, 8, dtype=torch.bfloat16)
+    w = torch.zeros(8, 4)
+    cu = torch.tensor([0, 16], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.conv1d_fwd(x, w, cu)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.conv1d_bwd(x, x, w, cu)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.conv1d_bwd_noalloc(x, x, w, cu)

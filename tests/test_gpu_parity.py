@@ -284,6 +284,32 @@ def test_binding_errors():
                        workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
 
 
+@pytest.mark.parametrize("case", ["weight_t", "dx_strided", "cu_int64", "dweight_shape",
+                                  "bias_shape", "host_bias", "dy_fp32"])
+def test_binding_rejects_layouts_the_kernels_do_not_read(case):
+    """Strides, dtypes and shapes are invisible behind the C ABI; the binding
+    refuses what the kernels would misread instead of passing its pointer on."""
+    w = synth.custom(64, 16, [64], seed=1, bias_dtype=torch.float32).to(DEV)
+    x, dy, W, cu, b = w.x, w.dy, w.weight, w.cu_seqlens, w.bias
+    dx = dW = None
+    if case == "weight_t":
+        W = W.t().contiguous().t()                       # [C, 4] view, column-major
+    elif case == "dx_strided":
+        dx = torch.empty(64, 32, dtype=torch.bfloat16, device=DEV)[:, :16]
+    elif case == "cu_int64":
+        cu = cu.long()
+    elif case == "dweight_shape":
+        dW = torch.empty(4, 16, device=DEV)
+    elif case == "bias_shape":
+        b = torch.zeros(8, device=DEV)
+    elif case == "host_bias":
+        b = b.cpu()
+    elif case == "dy_fp32":
+        dy = dy.float()
+    with pytest.raises((ValueError, TypeError)):
+        vcd.conv1d_bwd(x, dy, W, cu, b, "bf16", dx=dx, dweight=dW)
+
+
 def test_native_library_is_loaded():
     vcd.load_library()
     maps = open("/proc/self/maps").read()

@@ -88,9 +88,26 @@ def _dt(t):
     return _DTYPE[t.dtype]
 
 
-def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
+def _stream(stream, device):
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _require(t, name, dtypes, device, shape=None):
+    """The C ABI sees only a pointer: the layout the kernels assume is checked
+    here (CUDA, on x's device, contiguous, dtype, shape)."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, x on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must be one of {dtypes}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 def _sc(x):
@@ -134,12 +151,19 @@ def conv1d_fwd(x, weight, cu_seqlens, bias=None, y=None, workspace=None, stream=
     Returns y (allocated when not given)."""
     lib = load_library()
     S, C = _sc(x)
+    dev = x.device
+    _require(x, "x", (torch.bfloat16,), dev)
+    _require(weight, "weight", (torch.float32, torch.bfloat16), dev, (C, 4))
+    _require(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
+    _require(bias, "bias", (torch.float32, torch.bfloat16), dev, (C,))
     if y is None:
         y = torch.empty_like(x)
+    _require(y, "y", (torch.bfloat16,), dev, x.shape)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.conv1d_fwd(_ptr(x), S, C, _ptr(weight), _dt(weight), _ptr(cu_seqlens),
-                        cu_seqlens.numel() - 1, _ptr(bias), _dt(bias), _ptr(y), _ptr(workspace),
-                        nbytes, _stream(stream))
+    with torch.cuda.device(dev):
+        st = lib.conv1d_fwd(_ptr(x), S, C, _ptr(weight), _dt(weight), _ptr(cu_seqlens),
+                            cu_seqlens.numel() - 1, _ptr(bias), _dt(bias), _ptr(y),
+                            _ptr(workspace), nbytes, _stream(stream, dev))
     _check(st, "conv1d_fwd")
     return y
 
@@ -149,28 +173,40 @@ def conv1d_bwd(x, dy, weight, cu_seqlens, bias=None, policy="bf16", dx=None, dwe
     """Gradients of the forward: returns (dx, dweight, dbias or None).
 
     Output dtypes default to the parameters' dtypes. ``workspace`` (uint8, at
-    least conv1d_bwd_workspace_size(S, C) bytes) is allocated when omitted."""
+    least conv1d_bwd_route_workspace_size(S, C, policy) bytes) is allocated when
+    omitted."""
     lib = load_library()
     S, C = _sc(x)
     if policy not in POLICIES:
         raise ValueError(f"policy must be 'bf16' or 'fp32', got {policy!r}")
+    dev = x.device
+    _require(x, "x", (torch.bfloat16,), dev)
+    _require(dy, "dy", (torch.bfloat16,), dev, x.shape)
+    _require(weight, "weight", (torch.float32, torch.bfloat16), dev, (C, 4))
+    _require(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
+    _require(bias, "bias", (torch.float32, torch.bfloat16), dev, (C,))
     if dx is None:
         dx = torch.empty_like(x)
     if dweight is None:
-        dweight = torch.empty(C, 4, dtype=weight.dtype, device=x.device)
+        dweight = torch.empty(C, 4, dtype=weight.dtype, device=dev)
     if want_dbias is None:
         want_dbias = bias is not None
     if dbias is None and want_dbias:
         dbias = torch.empty(C, dtype=bias.dtype if bias is not None else torch.float32,
-                            device=x.device)
+                            device=dev)
+    _require(dx, "dx", (torch.bfloat16,), dev, x.shape)
+    _require(dweight, "dweight", (torch.float32, torch.bfloat16), dev, (C, 4))
+    _require(dbias, "dbias", (torch.float32, torch.bfloat16), dev, (C,))
     if workspace is None:
-        workspace = torch.empty(conv1d_bwd_workspace_size(S, C), dtype=torch.uint8,
-                                device=x.device)
+        workspace = torch.empty(conv1d_bwd_route_workspace_size(S, C, policy), dtype=torch.uint8,
+                                device=dev)
+    _require(workspace, "workspace", (torch.uint8,), dev)
     nbytes = workspace.numel() * workspace.element_size()
-    st = lib.conv1d_bwd(_ptr(x), _ptr(dy), S, C, _ptr(weight), _dt(weight), _ptr(cu_seqlens),
-                        cu_seqlens.numel() - 1, _ptr(bias), _dt(bias), POLICIES[policy],
-                        _ptr(dx), _ptr(dweight), _dt(dweight), _ptr(dbias), _dt(dbias),
-                        _ptr(workspace), nbytes, _stream(stream))
+    with torch.cuda.device(dev):
+        st = lib.conv1d_bwd(_ptr(x), _ptr(dy), S, C, _ptr(weight), _dt(weight), _ptr(cu_seqlens),
+                            cu_seqlens.numel() - 1, _ptr(bias), _dt(bias), POLICIES[policy],
+                            _ptr(dx), _ptr(dweight), _dt(dweight), _ptr(dbias), _dt(dbias),
+                            _ptr(workspace), nbytes, _stream(stream, dev))
     _check(st, "conv1d_bwd")
     return dx, dweight, dbias
 
@@ -185,18 +221,28 @@ def conv1d_bwd_noalloc(x, dy, weight, cu_seqlens, bias=None, policy="bf16", dx=N
     S, C = _sc(x)
     if policy not in POLICIES:
         raise ValueError(f"policy must be 'bf16' or 'fp32', got {policy!r}")
+    dev = x.device
+    _require(x, "x", (torch.bfloat16,), dev)
+    _require(dy, "dy", (torch.bfloat16,), dev, x.shape)
+    _require(weight, "weight", (torch.float32, torch.bfloat16), dev, (C, 4))
+    _require(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
+    _require(bias, "bias", (torch.float32, torch.bfloat16), dev, (C,))
     if dx is None:
         dx = torch.empty_like(x)
     if dweight is None:
-        dweight = torch.empty(C, 4, dtype=weight.dtype, device=x.device)
+        dweight = torch.empty(C, 4, dtype=weight.dtype, device=dev)
     if want_dbias is None:
         want_dbias = bias is not None
     if dbias is None and want_dbias:
         dbias = torch.empty(C, dtype=bias.dtype if bias is not None else torch.float32,
-                            device=x.device)
-    st = lib.conv1d_bwd_noalloc(_ptr(x), _ptr(dy), S, C, _ptr(weight), _dt(weight),
-                                _ptr(cu_seqlens), cu_seqlens.numel() - 1, _ptr(bias), _dt(bias),
-                                POLICIES[policy], _ptr(dx), _ptr(dweight), _dt(dweight),
-                                _ptr(dbias), _dt(dbias), _stream(stream))
+                            device=dev)
+    _require(dx, "dx", (torch.bfloat16,), dev, x.shape)
+    _require(dweight, "dweight", (torch.float32, torch.bfloat16), dev, (C, 4))
+    _require(dbias, "dbias", (torch.float32, torch.bfloat16), dev, (C,))
+    with torch.cuda.device(dev):
+        st = lib.conv1d_bwd_noalloc(_ptr(x), _ptr(dy), S, C, _ptr(weight), _dt(weight),
+                                    _ptr(cu_seqlens), cu_seqlens.numel() - 1, _ptr(bias),
+                                    _dt(bias), POLICIES[policy], _ptr(dx), _ptr(dweight),
+                                    _dt(dweight), _ptr(dbias), _dt(dbias), _stream(stream, dev))
     _check(st, "conv1d_bwd_noalloc")
     return dx, dweight, dbias
