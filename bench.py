@@ -150,10 +150,12 @@ def reduce_max(value, device):
     return float(t.item())
 
 
-def vcd_route_bytes(S, C, policy):
+def vcd_call_bytes(w, policy):
+    """Partial-row bytes the backward call writes (and its reduce reads back):
+    the exact workspace need of this call's launch shape."""
     import varlen_causal_depthwise_gb300 as vcd
 
-    return vcd.conv1d_bwd_route_workspace_size(S, C, policy)
+    return vcd.conv1d_bwd_call_workspace_size(w.S, w.C, w.num_docs, policy, w.bias is not None)
 
 
 def compulsory_bytes(S, C, partial_bytes):
@@ -303,9 +305,9 @@ def e2e_pipelined(w, policy, K, dev, vcd):
 def finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws, rank):
     import torch.distributed as dist
 
-    # the partial rows this route writes and reads back (the size query is the
-    # maximum over routes)
-    fwd_b, bwd_b = compulsory_bytes(S, C, vcd_route_bytes(S, C, policy))
+    # the partial rows this call writes and reads back (the workspace size
+    # query is the maximum over routes and launch shapes)
+    fwd_b, bwd_b = compulsory_bytes(S, C, vcd_call_bytes(w, policy))
     step_b = fwd_b + bwd_b
     ms_step = total_ms / K
     peak, peak_kind = measured_peak()

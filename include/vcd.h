@@ -70,12 +70,24 @@ int conv1d_fwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
  * as the forward query. */
 int conv1d_bwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
 
-/* Bytes of backward workspace one route needs: the partial rows of the
- * "bf16" (policy 0) or "fp32" (policy 1) program for (S, C); at most
- * conv1d_bwd_workspace_size(S, C). A conv1d_bwd call of that policy accepts
- * a workspace of this size. Errors as the queries above, plus
- * VCD_ERR_INVALID_ARG for an unknown policy. */
+/* Bytes of backward workspace one policy needs: the partial rows of the
+ * "bf16" (policy 0) or "fp32" (policy 1) program for (S, C), the larger of
+ * its two launch shapes; at most conv1d_bwd_workspace_size(S, C). Every
+ * conv1d_bwd call of that policy accepts a workspace of this size. Errors as
+ * the queries above, plus VCD_ERR_INVALID_ARG for an unknown policy. */
 int conv1d_bwd_route_workspace_size(int64_t S, int64_t C, int policy, size_t* bytes);
+
+/* Bytes of backward workspace one call needs, exactly: the partial rows that
+ * conv1d_bwd writes and reads for these arguments (has_bias: a bias is
+ * passed). The call picks one of two launch shapes from them -- 16 warps per
+ * SM for the "fp32" policy, for documents shorter than 32 tokens on average
+ * (num_docs * 32 >= S) and for calls without a bias; 12 warps with more
+ * registers otherwise -- and the shape sets the number of work units. At most
+ * conv1d_bwd_route_workspace_size(S, C, policy). Errors as
+ * conv1d_bwd_route_workspace_size, plus VCD_ERR_INVALID_ARG for S > 0 with
+ * num_docs <= 0. */
+int conv1d_bwd_call_workspace_size(int64_t S, int64_t C, int64_t num_docs, int policy,
+                                   int has_bias, size_t* bytes);
 
 /* Forward (forward page, Returns):
  *   y[t, c] = bf16(silu(sum_k weight[c, k] * x[t - 3 + k, c] + bias[c]))
@@ -131,7 +143,8 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C,
 
 /* Size of the fixed device scratch used by conv1d_bwd_noalloc: 8 MiB. Under
  * the "bf16" policy that holds the partial rows of every shape with
- * C <= 419328 (about 6 MB at most below that); the "fp32" policy uses one row
+ * C <= 419328 (at most 2432 rows of 2560 bytes, 6.2 MB, while C <= 311296;
+ * one row per 128-channel column above that); the "fp32" policy uses one row
  * per 256 tokens of each 128-channel column (2560 bytes each), so it fits
  * while ceil(S / 256) * ceil(C / 128) <= 3276, e.g. S <= 17408 at C = 6144. */
 #define VCD_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -57,9 +57,34 @@ def test_workspace_queries(lib):
             vcd.conv1d_bwd_workspace_size(*bad)
     bf, fp = (vcd.conv1d_bwd_route_workspace_size(65536, 6144, p) for p in ("bf16", "fp32"))
     assert bf < fp == n
-    assert bf == 48 * 50 * 128 * 5 * 4        # one row per warp-sized unit (2400 units)
+    # one row per warp-sized unit; the larger of the policy's two launch shapes
+    # (16 warps per SM: 48 columns x 50 rows = 2400 units)
+    assert bf == 48 * 50 * 128 * 5 * 4
     with pytest.raises(ValueError):
         vcd.conv1d_bwd_route_workspace_size(8, 8, "fp16")
+
+
+def test_call_workspace_query_follows_the_launch_shape(lib):
+    """The per-call query gives the partial rows of the launch shape the call
+    takes: 12 warps per SM (1824 target units) for the "bf16" policy with a
+    bias and documents of 32 tokens or more on average, 16 warps (2432)
+    otherwise; never more than the policy's query."""
+    S, C, row = 65536, 6144, 128 * 5 * 4
+    call = vcd.conv1d_bwd_call_workspace_size
+    assert call(S, C, 20, "bf16", True) == 48 * 38 * row           # wide: 1824 units
+    assert call(S, C, 20, "bf16", False) == 48 * 50 * row          # deep: 2400 units
+    assert call(S, C, S // 32, "bf16", True) == 48 * 50 * row      # short documents: deep
+    assert call(S, C, S // 32 - 1, "bf16", True) == 48 * 38 * row
+    assert call(S, C, 20, "fp32", True) == call(S, C, 20, "fp32", False) == 48 * 256 * row
+    for S_, C_, nd in ((4096, 256, 4), (131072, 1032, 52000), (300, 40, 3), (1, 8, 1)):
+        for pol in ("bf16", "fp32"):
+            for hb in (True, False):
+                assert 0 < call(S_, C_, nd, pol, hb) <= vcd.conv1d_bwd_route_workspace_size(S_, C_, pol)
+    assert call(0, 8, 0, "bf16", True) == 0
+    with pytest.raises(vcd.VcdError):
+        call(8, 8, 0, "bf16", True)          # tokens but no documents
+    with pytest.raises(ValueError):
+        call(8, 8, 1, "fp16", True)
 
 
 def _fwd(lib, **kw):

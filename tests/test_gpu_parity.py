@@ -121,7 +121,8 @@ def sample_points(w, n_random, rng):
     starts = np.unique(cu[:-1][cu[:-1] < S])
     special = np.concatenate([
         starts[:40], starts[-10:], (starts[:20] + 1), (starts[:20] + 2), (starts[:20] + 3),
-        _unit_edges(S, C, 4, 152 * 24), _unit_edges(S, C, 4, 152 * 16), [0, 1, 2, S - 3, S - 2, S - 1]])
+        _unit_edges(S, C, 4, 152 * 24), _unit_edges(S, C, 4, 152 * 12),
+        _unit_edges(S, C, 4, 152 * 16), [0, 1, 2, S - 3, S - 2, S - 1]])
     special = np.unique(np.clip(special, 0, S - 1))
     ch = np.unique(np.concatenate([[0, 1, 7, 8, C - 8, C - 1, 127, 128, 255, 256],
                                    rng.integers(0, C, 6)]))
@@ -192,6 +193,33 @@ def test_gradients_bitwise_reproducible(name):
             assert torch.equal(u.view(torch.int16) if u.dtype == torch.bfloat16 else u.view(torch.int32),
                                v.view(torch.int16) if v.dtype == torch.bfloat16 else v.view(torch.int32))
             assert torch.equal(u, z)
+
+
+@pytest.mark.parametrize("name,S,pol,bias", [("linattn", 8192, "bf16", True),
+                                              ("mid", 8192, "bf16", False),
+                                              ("boundary", 8192, "bf16", True),
+                                              ("boundary", 8192, "fp32", True)])
+def test_exact_call_workspace(name, S, pol, bias):
+    """A workspace of exactly conv1d_bwd_call_workspace_size bytes is accepted
+    and gives the same bits as the full-size one; 16 bytes less is refused
+    before anything is launched."""
+    w = synth.make(name, device=DEV, S=S)
+    b = w.bias if bias else None
+    n = vcd.conv1d_bwd_call_workspace_size(w.S, w.C, w.num_docs, pol, b is not None)
+    assert 0 < n <= vcd.conv1d_bwd_route_workspace_size(w.S, w.C, pol)
+    full = vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, b, pol,
+                          dweight=torch.empty(w.C, 4, device=DEV),
+                          dbias=None if b is None else torch.empty(w.C, device=DEV))
+    exact = vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, b, pol,
+                           dweight=torch.empty(w.C, 4, device=DEV),
+                           dbias=None if b is None else torch.empty(w.C, device=DEV),
+                           workspace=torch.empty(n, dtype=torch.uint8, device=DEV))
+    torch.cuda.synchronize()
+    for u, v in zip(full, exact):
+        assert (u is None and v is None) or torch.equal(u, v)
+    with pytest.raises(vcd.VcdError, match="workspace"):
+        vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, b, pol,
+                       workspace=torch.empty(n - 16, dtype=torch.uint8, device=DEV))
 
 
 def _guarded(n, dtype, guard=64, fill=None):

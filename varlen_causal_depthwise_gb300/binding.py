@@ -30,6 +30,7 @@ SIGNATURES = {
     "conv1d_fwd_workspace_size": (_int, [_i64, _i64, ctypes.POINTER(_sz)]),
     "conv1d_bwd_workspace_size": (_int, [_i64, _i64, ctypes.POINTER(_sz)]),
     "conv1d_bwd_route_workspace_size": (_int, [_i64, _i64, _int, ctypes.POINTER(_sz)]),
+    "conv1d_bwd_call_workspace_size": (_int, [_i64, _i64, _i64, _int, _int, ctypes.POINTER(_sz)]),
     "conv1d_fwd": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _vp, _vp, _sz,
                           _vp]),
     "conv1d_bwd": (_int, [_vp, _vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _int, _vp,
@@ -143,6 +144,18 @@ def conv1d_bwd_route_workspace_size(S, C, policy="bf16"):
     return n.value
 
 
+def conv1d_bwd_call_workspace_size(S, C, num_docs, policy="bf16", has_bias=True):
+    """Bytes one backward call needs exactly (its launch shape's partial rows)."""
+    if policy not in POLICIES:
+        raise ValueError(f"policy must be 'bf16' or 'fp32', got {policy!r}")
+    n = ctypes.c_size_t(0)
+    _check(load_library().conv1d_bwd_call_workspace_size(int(S), int(C), int(num_docs),
+                                                         POLICIES[policy], int(bool(has_bias)),
+                                                         ctypes.byref(n)),
+           "conv1d_bwd_call_workspace_size")
+    return n.value
+
+
 def conv1d_fwd(x, weight, cu_seqlens, bias=None, y=None, workspace=None, stream=None):
     """y = bf16(silu(causal width-4 depthwise conv(x) + bias)), per document.
 
@@ -173,8 +186,9 @@ def conv1d_bwd(x, dy, weight, cu_seqlens, bias=None, policy="bf16", dx=None, dwe
     """Gradients of the forward: returns (dx, dweight, dbias or None).
 
     Output dtypes default to the parameters' dtypes. ``workspace`` (uint8, at
-    least conv1d_bwd_route_workspace_size(S, C, policy) bytes) is allocated when
-    omitted."""
+    least conv1d_bwd_call_workspace_size(S, C, num_docs, policy, bias is not
+    None) bytes; conv1d_bwd_route_workspace_size(S, C, policy) always suffices)
+    is allocated when omitted."""
     lib = load_library()
     S, C = _sc(x)
     if policy not in POLICIES:

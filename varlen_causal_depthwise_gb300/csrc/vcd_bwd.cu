@@ -13,7 +13,7 @@
 // Main kernel: one warp per work unit (32 * kBwdVec channels x L tokens,
 // vcd_plan.h),
 // walking its tokens forward once. x and dy stream through a per-warp
-// shared-memory ring (cp.async, one batch of kBwdU tokens ahead). Registers
+// shared-memory ring (cp.async, kBwdNs - 1 batches of kBwdU tokens ahead). Registers
 // hold the x of the three previous tokens and their dpre, so each token gives
 // pre, dpre, its dweight / dbias products, and dx of the token three back in
 // gather form: dx[t-3] = w3 dpre[t-3] + w2 dpre[t-2] + w1 dpre[t-1] + w0 dpre[t].
@@ -39,12 +39,6 @@
 namespace vcd {
 namespace {
 
-#ifndef VCD_BWD_U
-#define VCD_BWD_U 12
-#endif
-#ifndef VCD_BWD_NS
-#define VCD_BWD_NS 2
-#endif
 #ifndef VCD_BWD_PACKED
 #define VCD_BWD_PACKED 0
 #endif
@@ -53,16 +47,26 @@ namespace {
 #endif
 constexpr bool kPK = VCD_BWD_PACKED != 0;                 // packed FP32x2 arithmetic
 constexpr bool kPA = kPK || VCD_BWD_PACKED_ACC != 0;      // ... for dweight / dbias / dx
-constexpr int kBwdU = VCD_BWD_U;                          // tokens per batch (even, <= 30)
-constexpr int kBwdNs = VCD_BWD_NS;                        // ring stages (>= 2)
 constexpr int kNP = kBwdVec / 2;                          // channel pairs per lane
 constexpr int kBwdColCh = 32 * kBwdVec;                   // channels per unit column
 constexpr int kBwdRowBytes = 2 * kBwdColCh;               // bytes of a token's row segment
-constexpr int kBwdTensorBytes = kBwdU * kBwdRowBytes;     // one tensor's rows of one stage
-constexpr int kBwdStageBytes = 2 * kBwdTensorBytes;       // x rows, then dy rows
-constexpr int kBwdWarpBytes = kBwdNs * kBwdStageBytes;
-constexpr int kBwdSmemBytes = kBwdWarpsPerCta * kBwdWarpBytes;
-static_assert(kBwdU % 2 == 0 && kBwdU <= 30 && kBwdNs >= 2, "batch geometry");
+
+// Geometry of a launch shape (vcd_plan.h): warps per CTA (one CTA per SM),
+// ring stages and tokens per batch.
+template <int SHAPE> struct BwdGeom;
+template <> struct BwdGeom<kBwdWide> { static constexpr int kWarps = 12, kNs = 3, kU = 12; };
+template <> struct BwdGeom<kBwdDeep> { static constexpr int kWarps = 16, kNs = 2, kU = 8; };
+template <int SHAPE> struct BwdShapeT : BwdGeom<SHAPE> {
+    using G = BwdGeom<SHAPE>;
+    static constexpr int kThreads = 32 * G::kWarps;
+    static constexpr int kTensorBytes = G::kU * kBwdRowBytes;   // one tensor's rows of one stage
+    static constexpr int kStageBytes = 2 * kTensorBytes;        // x rows, then dy rows
+    static constexpr int kWarpBytes = G::kNs * kStageBytes;
+    static constexpr int kSmemBytes = G::kWarps * kWarpBytes;
+    static_assert(G::kU % 2 == 0 && G::kU <= 30 && G::kNs >= 2, "batch geometry");
+    static_assert(kSmemBytes <= 227 * 1024, "ring exceeds the shared memory of one CTA");
+    static_assert(kBwdShapeWarps[SHAPE] == G::kWarps, "plan and kernel disagree on the shape");
+};
 
 constexpr int kPolicyBF16 = 0;
 constexpr int kPolicyFP32 = 1;
@@ -78,15 +82,18 @@ __device__ __forceinline__ float2 grad_at(float2 pre) {
 // SEG: a warp's chunk holds several units (the "fp32" policy's short units);
 // without it every chunk is a single unit and the unit-boundary logic compiles
 // away.
-template <bool W_BF16, int BIAS, int POLICY, bool SEG>
-__global__ void __launch_bounds__(kBwdThreadsPerCta, kBwdCtasPerSm) bwd_main_kernel(const BwdArgs a) {
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG>
+__global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel(const BwdArgs a) {
+    using SH = BwdShapeT<SHAPE>;
+    constexpr int kBwdU = SH::kU, kBwdNs = SH::kNs;
+    constexpr int kBwdTensorBytes = SH::kTensorBytes, kBwdStageBytes = SH::kStageBytes;
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
-    unsigned char* const ring = smem + wid * kBwdWarpBytes;
+    unsigned char* const ring = smem + wid * SH::kWarpBytes;
     const uint32_t ring_s = smem_u32(ring);
-    const int64_t warp0 = (int64_t)blockIdx.x * kBwdWarpsPerCta + wid;
-    const int64_t nwarps = (int64_t)gridDim.x * kBwdWarpsPerCta;
+    const int64_t warp0 = (int64_t)blockIdx.x * SH::kWarps + wid;
+    const int64_t nwarps = (int64_t)gridDim.x * SH::kWarps;
     const int64_t S = a.plan.S, C = a.plan.C, L = a.plan.L;
     const int64_t units = a.plan.units, ncols = a.plan.ncols;
     const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(a.x);
@@ -372,45 +379,47 @@ __global__ void __launch_bounds__(kRedOutputs * kRedSlices) bwd_reduce_kernel(co
 
 // -------------------------------------------------------------- launch ---
 
-template <bool W_BF16, int BIAS, int POLICY, bool SEG>
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG>
 int prepare_main_t() {
     // Once per (instantiation, device): allow the dynamic shared memory and
     // read the occupancy; both are host-side queries.
+    using SH = BwdShapeT<SHAPE>;
     static int occ[kMaxDevices] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     if (occ[dev] > 0) return occ[dev];
-    if (cudaFuncSetAttribute(bwd_main_kernel<W_BF16, BIAS, POLICY, SEG>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SH::kSmemBytes) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<W_BF16, BIAS, POLICY, SEG>,
-                                                      kBwdThreadsPerCta, kBwdSmemBytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>,
+                                                      SH::kThreads, SH::kSmemBytes) != cudaSuccess)
         return 0;
     occ[dev] = n;
     return n;
 }
 
-template <bool W_BF16, int BIAS, int POLICY>
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY>
 cudaError_t launch_main_t(const BwdArgs& a, int sm_count, cudaStream_t stream) {
+    using SH = BwdShapeT<SHAPE>;
     // Occupancy is the same for both forms (same launch bounds and shared memory).
-    const int occ = prepare_main_t<W_BF16, BIAS, POLICY, false>();
-    if (occ <= 0 || prepare_main_t<W_BF16, BIAS, POLICY, true>() <= 0)
+    const int occ = prepare_main_t<SHAPE, W_BF16, BIAS, POLICY, false>();
+    if (occ <= 0 || prepare_main_t<SHAPE, W_BF16, BIAS, POLICY, true>() <= 0)
         return cudaErrorInvalidConfiguration;
-    const int64_t ctas_needed = (a.plan.units + kBwdWarpsPerCta - 1) / kBwdWarpsPerCta;
+    const int64_t ctas_needed = (a.plan.units + SH::kWarps - 1) / SH::kWarps;
     const int64_t resident = (int64_t)sm_count * occ;
     const int64_t grid = ctas_needed < resident ? ctas_needed : resident;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
-    cfg.blockDim = dim3(kBwdThreadsPerCta);
-    cfg.dynamicSmemBytes = kBwdSmemBytes;
+    cfg.blockDim = dim3(SH::kThreads);
+    cfg.dynamicSmemBytes = SH::kSmemBytes;
     cfg.stream = stream;
     // the kernel cuts each column into chunks of `per` rows, one per warp
-    const int64_t nwarps = (int64_t)cfg.gridDim.x * kBwdWarpsPerCta;
+    const int64_t nwarps = (int64_t)cfg.gridDim.x * SH::kWarps;
     const int64_t wpc = nwarps / a.plan.ncols > 0 ? nwarps / a.plan.ncols : 1;
     const int64_t per = (a.plan.rows + wpc - 1) / wpc;
-    if (per > 1) return cudaLaunchKernelEx(&cfg, bwd_main_kernel<W_BF16, BIAS, POLICY, true>, a);
-    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<W_BF16, BIAS, POLICY, false>, a);
+    if (per > 1) return cudaLaunchKernelEx(&cfg, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, true>, a);
+    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, false>, a);
 }
 
 template <typename ACC>
@@ -432,15 +441,21 @@ cudaError_t launch_reduce_t(const BwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_bwd(const BwdArgs& a, int sm_count, cudaStream_t stream) {
     typedef cudaError_t (*L)(const BwdArgs&, int, cudaStream_t);
-#define VCD_ROW(WB, POL) {launch_main_t<WB, kBiasNone, POL>, launch_main_t<WB, kBiasF32, POL>, launch_main_t<WB, kBiasBF16, POL>}
-    static const L launch[2][2][3] = {{VCD_ROW(false, kPolicyBF16), VCD_ROW(false, kPolicyFP32)},
-                                      {VCD_ROW(true, kPolicyBF16), VCD_ROW(true, kPolicyFP32)}};
+#define VCD_ROW(SH, WB, POL) {launch_main_t<SH, WB, kBiasNone, POL>, launch_main_t<SH, WB, kBiasF32, POL>, \
+                              launch_main_t<SH, WB, kBiasBF16, POL>}
+    // [weight dtype][bias kind]; the "fp32" policy runs the deep shape only
+    static const L wide_bf16[2][3] = {VCD_ROW(kBwdWide, false, kPolicyBF16), VCD_ROW(kBwdWide, true, kPolicyBF16)};
+    static const L deep_bf16[2][3] = {VCD_ROW(kBwdDeep, false, kPolicyBF16), VCD_ROW(kBwdDeep, true, kPolicyBF16)};
+    static const L deep_fp32[2][3] = {VCD_ROW(kBwdDeep, false, kPolicyFP32), VCD_ROW(kBwdDeep, true, kPolicyFP32)};
 #undef VCD_ROW
     const int wi = a.weight_bf16 ? 1 : 0;
-    const int pi = a.policy == kPolicyFP32 ? 1 : 0;
-    cudaError_t e = launch[wi][pi][a.bias_kind](a, sm_count, stream);
+    const bool fp32 = a.policy == kPolicyFP32;
+    if (fp32 && a.shape != kBwdDeep) return cudaErrorInvalidValue;
+    const L fn = fp32 ? deep_fp32[wi][a.bias_kind]
+                      : a.shape == kBwdWide ? wide_bf16[wi][a.bias_kind] : deep_bf16[wi][a.bias_kind];
+    cudaError_t e = fn(a, sm_count, stream);
     if (e != cudaSuccess) return e;
-    return pi ? launch_reduce_t<double>(a, stream) : launch_reduce_t<float>(a, stream);
+    return fp32 ? launch_reduce_t<double>(a, stream) : launch_reduce_t<float>(a, stream);
 }
 
 }  // namespace vcd

@@ -77,6 +77,14 @@ int conv1d_bwd_route_workspace_size(int64_t S, int64_t C, int policy, size_t* by
     return VCD_OK;
 }
 
+int conv1d_bwd_call_workspace_size(int64_t S, int64_t C, int64_t num_docs, int policy,
+                                   int has_bias, size_t* bytes) {
+    if (!bytes || check_shape(S, C, num_docs) != VCD_OK) return VCD_ERR_INVALID_ARG;
+    if (policy != VCD_SILU_GRAD_BF16 && policy != VCD_SILU_GRAD_FP32) return VCD_ERR_INVALID_ARG;
+    *bytes = (size_t)vcd::bwd_call_workspace_bytes(S, C, num_docs, policy, has_bias != 0);
+    return VCD_OK;
+}
+
 int conv1d_fwd(const void* x, int64_t S, int64_t C, const void* weight, int weight_dtype,
                const int32_t* cu_seqlens, int64_t num_docs, const void* bias, int bias_dtype,
                void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -131,7 +139,10 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* 
     if (!dy || !dx) return VCD_ERR_INVALID_ARG;
     if (!aligned(dy, 16) || !aligned(dx, 16)) return VCD_ERR_MISALIGNED;
     if (dx == x || dx == dy) return VCD_ERR_INVALID_ARG;
-    const uint64_t need = vcd::bwd_workspace_bytes_for(S, C, policy);   // this route's rows
+    const int weight_bf16 = weight_dtype == VCD_BF16;
+    const int bias_kind = !bias ? vcd::kBiasNone : bias_dtype == VCD_BF16 ? vcd::kBiasBF16 : vcd::kBiasF32;
+    const int shape = vcd::bwd_shape(S, num_docs, policy, bias != nullptr);
+    const uint64_t need = vcd::bwd_workspace_bytes_for(S, C, policy, shape);   // this route's rows
     if (!workspace || workspace_bytes < need) return VCD_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 16)) return VCD_ERR_MISALIGNED;
     int sms = 0;
@@ -148,12 +159,13 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* 
     a.partials = static_cast<float*>(workspace);
     a.dweight = dweight;
     a.dbias = dbias;
-    a.weight_bf16 = weight_dtype == VCD_BF16;
-    a.bias_kind = !bias ? vcd::kBiasNone : bias_dtype == VCD_BF16 ? vcd::kBiasBF16 : vcd::kBiasF32;
+    a.weight_bf16 = weight_bf16;
+    a.bias_kind = bias_kind;
     a.policy = policy;
     a.dweight_bf16 = dweight_dtype == VCD_BF16;
     a.dbias_bf16 = dbias_dtype == VCD_BF16;
-    a.plan = vcd::bwd_plan(S, C, policy);
+    a.shape = shape;
+    a.plan = vcd::bwd_plan(S, C, policy, shape);
     return cuda_status(vcd::launch_bwd(a, sms, stream));
 }
 

@@ -40,7 +40,8 @@ struct BwdArgs {
     int policy;               // 0: SiLU' at bf16(pre), 1: at the FP32 pre
     int dweight_bf16;
     int dbias_bf16;
-    Plan plan;                // bwd_plan(S, C)
+    int shape;                // BwdShape
+    Plan plan;                // bwd_plan(S, C, policy, shape)
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, int sm_count, cudaStream_t stream);

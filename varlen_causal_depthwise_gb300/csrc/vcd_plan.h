@@ -1,16 +1,18 @@
 // vcd_plan.h -- how the [S, C] token x channel plane is cut into work units.
 //
-// A lane owns VEC consecutive channels (2 * VEC bytes of BF16 per token: 4
-// channels in the forward, 2 in the backward, whose per-lane state is larger);
-// a warp owns 32 lanes, i.e. one row segment of 32 * VEC channels per token; a
-// "column" is those channels, a "row" a run of L consecutive tokens, and a
-// unit is one (row, column) pair, processed by one warp token by token with a
-// 3-token halo on the left (and on the right in the backward).
+// A lane owns VEC consecutive channels (2 * VEC bytes of BF16 per token, 4
+// channels in both directions); a warp owns 32 lanes, i.e. one row segment of
+// 32 * VEC channels per token; a "column" is those channels, a "row" a run of
+// L consecutive tokens, and a unit is one (row, column) pair, processed by one
+// warp token by token with a 3-token halo on the left (and on the right in the
+// backward).
 //
-// The cut is a function of (S, C) and compile-time constants only -- never of
-// the device -- so the backward's partial rows, and therefore its fixed-order
-// reduction, are the same on every GPU: gradients are bitwise reproducible
-// per (S, C, route). The unit counts are sized so that one wave of the
+// The cut is a function of (S, C), the backward's launch shape and
+// compile-time constants only -- never of the device -- so the backward's
+// partial rows, and therefore its fixed-order reduction, are the same on every
+// GPU: gradients are bitwise reproducible per (S, C, route), where the route
+// (weight / bias dtypes, SiLU' policy, launch shape) is chosen on the host from
+// the call's arguments. The unit counts are sized so that one wave of the
 // persistent grid takes every unit on GB300 (152 SMs x the kernel's resident
 // warps per SM).
 #pragma once
@@ -31,19 +33,37 @@ constexpr int kPartialStride = 5;             // dweight[0..3], dbias per channe
 #ifndef VCD_FWD_CTAS_PER_SM
 #define VCD_FWD_CTAS_PER_SM 3
 #endif
-#ifndef VCD_BWD_CTAS_PER_SM
-#define VCD_BWD_CTAS_PER_SM 2
-#endif
 constexpr int kFwdCtasPerSm = VCD_FWD_CTAS_PER_SM;
-constexpr int kBwdCtasPerSm = VCD_BWD_CTAS_PER_SM;
 constexpr int64_t kGb300Sms = 152;
 constexpr int64_t kFwdTargetUnits = kGb300Sms * kFwdCtasPerSm * kWarpsPerCta;
-#ifndef VCD_BWD_WARPS_PER_CTA
-#define VCD_BWD_WARPS_PER_CTA 8
-#endif
-constexpr int kBwdWarpsPerCta = VCD_BWD_WARPS_PER_CTA;
-constexpr int kBwdThreadsPerCta = 32 * kBwdWarpsPerCta;
-constexpr int64_t kBwdTargetUnits = kGb300Sms * kBwdCtasPerSm * kBwdWarpsPerCta;
+
+// Backward launch shapes: one CTA per SM either way; they trade registers for
+// warps.
+//   kBwdWide: 12 warps, up to 168 registers a thread -- mask-free streaming
+//             whose 16-warp build would spill;
+//   kBwdDeep: 16 warps, up to 128 registers a thread -- more warps to hide the
+//             latency of instruction-heavy paths (document masks in most
+//             batches, the "fp32" policy's SiLU').
+// bwd_shape() picks one per call.
+enum BwdShape { kBwdWide = 0, kBwdDeep = 1 };
+constexpr int kBwdShapeWarps[2] = {12, 16};
+
+// Mean document length (tokens) below which most batches hold a document
+// start and take the masked path.
+constexpr int64_t kShortDocTokens = 32;
+
+// The backward's launch shape for a call: deep for the "fp32" policy and for
+// short documents (instruction-heavy paths, where more warps hide more
+// latency); under the "bf16" policy with longer documents, deep when the route
+// has no bias -- those kernels keep all their state within 128 registers --
+// and wide with a bias, whose 16-warp kernels would spill registers. A
+// function of the call's arguments only, so a route's partial rows are the
+// same on every call and every device.
+inline int bwd_shape(int64_t S, int64_t num_docs, int policy, bool has_bias) {
+    if (policy == 1) return kBwdDeep;
+    if (num_docs * kShortDocTokens >= S) return kBwdDeep;
+    return has_bias ? kBwdWide : kBwdDeep;
+}
 
 struct Plan {
     int64_t S, C;
@@ -83,8 +103,8 @@ inline Plan fwd_plan(int64_t S, int64_t C) { return make_plan(S, C, kFwdVec, kFw
 #endif
 constexpr int64_t kFp32TokensPerUnit = VCD_FP32_UNIT_TOKENS;
 
-inline Plan bwd_plan(int64_t S, int64_t C, int policy) {
-    Plan p = make_plan(S, C, kBwdVec, kBwdTargetUnits);
+inline Plan bwd_plan(int64_t S, int64_t C, int policy, int shape) {
+    Plan p = make_plan(S, C, kBwdVec, kGb300Sms * kBwdShapeWarps[shape]);
     if (policy == 1 && p.L > kFp32TokensPerUnit && S > 0) {
         p.L = kFp32TokensPerUnit;
         p.rows = (S + p.L - 1) / p.L;
@@ -95,13 +115,28 @@ inline Plan bwd_plan(int64_t S, int64_t C, int policy) {
 
 // Bytes of one route's partial rows: one FP32 row of 32 * kBwdVec channels x
 // 5 values per unit.
-inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy) {
+inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy, int shape) {
     if (S <= 0) return 0;
-    const Plan p = bwd_plan(S, C, policy);
+    const Plan p = bwd_plan(S, C, policy, shape);
     return (uint64_t)p.units * p.col_channels * kPartialStride * sizeof(float);
 }
 
-// The most any route needs (the "fp32" policy's plan has at least as many units).
+// The most a policy's routes need over every call shape: the "fp32" policy
+// always runs the deep shape, the "bf16" policy either shape.
+inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy) {
+    const uint64_t d = bwd_workspace_bytes_for(S, C, policy, kBwdDeep);
+    if (policy == 1) return d;
+    const uint64_t w = bwd_workspace_bytes_for(S, C, policy, kBwdWide);
+    return w > d ? w : d;
+}
+
+// What one call needs.
+inline uint64_t bwd_call_workspace_bytes(int64_t S, int64_t C, int64_t num_docs, int policy,
+                                         bool has_bias) {
+    return bwd_workspace_bytes_for(S, C, policy, bwd_shape(S, num_docs, policy, has_bias));
+}
+
+// The most any route needs.
 inline uint64_t bwd_workspace_bytes(int64_t S, int64_t C) {
     const uint64_t a = bwd_workspace_bytes_for(S, C, 0), b = bwd_workspace_bytes_for(S, C, 1);
     return a > b ? a : b;
