@@ -135,11 +135,32 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
         int64_t cur_row = row0;                                   // unit being accumulated
         int r_next = SEG && row1 - row0 > 1 ? 3 + Li : INT_MAX;   // where the next unit starts
 
+        // The first batches' copies go out before the taps and the document
+        // lookup, whose dependent loads then overlap them.
+        RowStream<2, kBwdRowBytes, int> rs;                 // x over [q0, u_end), dy over [t_begin, u_end)
+        {
+            const __nv_bfloat16* const bases[2] = {x, dy};
+            const int64_t lows[2] = {q0 > 0 ? q0 : 0, t_begin};
+            rs.init(bases, C, col, q0, lows, u_end, lane);
+        }
+
+        __syncwarp();                    // the previous unit's reads of the ring are done
+        auto issue = [&](int i, int slot) {
+            if (i < nb) {
+                const uint32_t st = ring_s + slot * kBwdStageBytes;
+                const uint32_t d[2] = {st, st + kBwdTensorBytes};
+                rs.stage<kBwdU>(d, i * kBwdU, x);
+            }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int s = 0; s < kBwdNs - 1; ++s) issue(s, s);
+
         float2 w[4][kNP], b[kNP];
         load_taps<W_BF16, BIAS, kNP>(a.weight, a.bias, c0, active, w, b);
         DocCursor doc;
         doc.init(cu, ncu, (int)q0 - 2, lane);
-        uint32_t carry = doc.starts((int)q0 - 2, 2, lane);            // bits of q0-2, q0-1
+        uint32_t carry = doc.starts(cu, ncu, (int)q0 - 2, 2, lane);            // bits of q0-2, q0-1
 
         float2 xc[3][kNP], dc[3][kNP];    // x and dpre of tokens q-3, q-2, q-1
         float2 dw[4][kNP], db[kNP];       // this unit's FP32 sums
@@ -183,26 +204,8 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
             }
         };
 
-        RowStream<2, kBwdRowBytes> rs;                 // x over [q0, u_end), dy over [t_begin, u_end)
-        {
-            const __nv_bfloat16* const bases[2] = {x, dy};
-            const int64_t lows[2] = {q0 > 0 ? q0 : 0, t_begin};
-            rs.init(bases, C, col, q0, lows, u_end, lane);
-        }
         __nv_bfloat16* dxp = dx + (q0 - 3) * C + c0;   // dx row of relative token -3
         const int64_t dstep = C;
-
-        __syncwarp();                    // the previous unit's reads of the ring are done
-        auto issue = [&](int i, int slot) {
-            if (i < nb) {
-                const uint32_t st = ring_s + slot * kBwdStageBytes;
-                const uint32_t d[2] = {st, st + kBwdTensorBytes};
-                rs.stage<kBwdU>(d, i * kBwdU);
-            }
-            cp_async_commit();
-        };
-#pragma unroll
-        for (int s = 0; s < kBwdNs - 1; ++s) issue(s, s);
 
         int slot = 0;
         for (int i = 0; i < nb; ++i) {
@@ -211,12 +214,12 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
             issue(i + kBwdNs - 1, slot == 0 ? kBwdNs - 1 : slot - 1);
             const int r0 = i * kBwdU;
             const int64_t q = q0 + r0;
-            const uint32_t nw = doc.starts((int)q, kBwdU, lane);
+            const uint32_t nw = doc.starts(cu, ncu, (int)q, kBwdU, lane);
+            __nv_bfloat16* dxq = dxp + (int64_t)r0 * dstep;  // dx row of token q - 3
             const uint32_t M = carry | (nw << 2);            // bit i <-> token q - 2 + i
             carry = nw >> (kBwdU - 2);
             const unsigned char* sx = ring + slot * kBwdStageBytes + lane * (2 * kBwdVec);
             const unsigned char* sg = sx + kBwdTensorBytes;
-            __nv_bfloat16* dxq = dxp + (int64_t)r0 * dstep;  // dx row of token q - 3
 
             if (M == 0 && r0 >= 6 && r0 + kBwdU <= r_end && (!SEG || r_next >= r0 + kBwdU)) {
                 // every token accumulates and emits dx three tokens back

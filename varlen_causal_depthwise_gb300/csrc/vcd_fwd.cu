@@ -83,12 +83,12 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
         load_taps<W_BF16, BIAS, 2>(a.weight, a.bias, c0, active, w, b);
         DocCursor doc;
         doc.init(cu, ncu, (int)q0 - 2, lane);
-        uint32_t carry = doc.starts((int)q0 - 2, 2, lane);            // bits of q0-2, q0-1
+        uint32_t carry = doc.starts(cu, ncu, (int)q0 - 2, 2, lane);            // bits of q0-2, q0-1
         float2 xc[3][2];                                              // x[q-3], x[q-2], x[q-1]
 #pragma unroll
         for (int k = 0; k < 3; ++k) xc[k][0] = xc[k][1] = zero2();
 
-        RowStream<1, kFwdRowBytes> rs;
+        RowStream<1, kFwdRowBytes, int64_t> rs;
         {
             const __nv_bfloat16* const bases[1] = {x};
             const int64_t lows[1] = {q0 > 0 ? q0 : 0};
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
         for (int s = 0; s < kFwdNs - 1; ++s) {
             if (s < nb) {
                 const uint32_t d[1] = {ring_s + s * kFwdStageBytes};
-                rs.stage<kFwdU>(d, s * kFwdU);
+                rs.stage<kFwdU>(d, s * kFwdU, x);
             }
             cp_async_commit();
         }
@@ -116,13 +116,13 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
                 const int nslot = slot == 0 ? kFwdNs - 1 : slot - 1;   // (i + Ns - 1) % Ns
                 if (nx < nb) {
                     const uint32_t d[1] = {ring_s + nslot * kFwdStageBytes};
-                    rs.stage<kFwdU>(d, nx * kFwdU);
+                    rs.stage<kFwdU>(d, nx * kFwdU, x);
                 }
                 cp_async_commit();
             }
             const int r0 = i * kFwdU;                    // relative index of the batch
             const int64_t q = q0 + r0;
-            const uint32_t nw = doc.starts((int)q, kFwdU, lane);
+            const uint32_t nw = doc.starts(cu, ncu, (int)q, kFwdU, lane);
             const uint32_t M = carry | (nw << 2);        // bit i <-> token q - 2 + i
             carry = nw >> (kFwdU - 2);
             const unsigned char* st = ring + slot * kFwdStageBytes + lane * (2 * kFwdVec);
