@@ -336,18 +336,29 @@ template <> __device__ __forceinline__ void store_out<double>(void* base, int64_
 }
 
 // Reduce: output (channel c, value k) is the sum over the R unit rows of its
-// column. A CTA handles 32 outputs with 8 threads each: thread s sums the
-// fixed row slice [s R / 8, (s + 1) R / 8) in row order, then thread 0 of the
-// output adds the 8 slice sums in slice order. The order depends on R only, so
-// the result is bitwise reproducible per (S, C, route).
+// column. A CTA handles 32 outputs with n threads each (n = red_slices(R)):
+// thread s sums the fixed row slice [s R / n, (s + 1) R / n) in row order,
+// then thread 0 of the output adds the n slice sums in slice order. The order
+// depends on R only, so the result is bitwise reproducible per (S, C, route).
+// n grows with R (at least 8 rows a slice, at most 16 slices) so that each
+// thread's chain of dependent loads stays short: the "bf16" policy has a few
+// dozen rows per column (8 slices), the "fp32" policy one per 256 tokens
+// (1024 at S = 262144: 16 slices of 64 rows).
 constexpr int kRedOutputs = 32;
-constexpr int kRedSlices = 8;
+constexpr int kRedMaxSlices = 16;
+
+inline int red_slices(int64_t rows) {
+    int n = 1;
+    while (n < kRedMaxSlices && rows >= 8 * (int64_t)n) n *= 2;
+    return n;
+}
 
 template <typename ACC>
-__global__ void __launch_bounds__(kRedOutputs * kRedSlices) bwd_reduce_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kRedOutputs * kRedMaxSlices, 4) bwd_reduce_kernel(const BwdArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    __shared__ ACC part[kRedSlices][kRedOutputs];
+    __shared__ ACC part[kRedMaxSlices][kRedOutputs];
     const Plan& P = a.plan;
+    const int nsl = blockDim.x / kRedOutputs;
     const int o = threadIdx.x % kRedOutputs;          // consecutive threads: consecutive outputs
     const int sl = threadIdx.x / kRedOutputs;
     const int64_t idx = (int64_t)blockIdx.x * kRedOutputs + o;
@@ -357,25 +368,29 @@ __global__ void __launch_bounds__(kRedOutputs * kRedSlices) bwd_reduce_kernel(co
     const int64_t col = c / kBwdColCh, ci = c % kBwdColCh;
     const float* src = a.partials + (col * kBwdColCh + ci) * kPartialStride + k;
     const int64_t stride = P.ncols * kBwdColCh * kPartialStride;
-    const int64_t r0 = P.rows * sl / kRedSlices, r1 = P.rows * (sl + 1) / kRedSlices;
+    const int64_t r0 = P.rows * sl / nsl, r1 = P.rows * (sl + 1) / nsl;
     ACC acc = 0;
     if (valid && !(k == 4 && a.dbias == nullptr)) {
-        int64_t r = r0;
-        for (; r + 4 <= r1; r += 4) {
-            float v[4];
+        // batches of 8 independent loads; rows past r1 read nothing and add
+        // zero, which leaves every sum and its order unchanged
+        const int n = (int)(r1 - r0);
+        const float* q = src + r0 * stride;
+        for (int r = 0; r < n; r += 8) {
+            float v[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = __ldcg(src + (r + j) * stride);
+            for (int j = 0; j < 8; ++j) {
+                v[j] = r + j < n ? __ldcg(q) : 0.0f;
+                q += stride;
+            }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc += (ACC)v[j];
+            for (int j = 0; j < 8; ++j) acc += (ACC)v[j];
         }
-        for (; r < r1; ++r) acc += (ACC)__ldcg(src + r * stride);
     }
     part[sl][o] = acc;
     __syncthreads();
     if (sl != 0 || !valid || (k == 4 && a.dbias == nullptr)) return;
     ACC total = part[0][o];
-#pragma unroll
-    for (int j = 1; j < kRedSlices; ++j) total += part[j][o];
+    for (int j = 1; j < nsl; ++j) total += part[j][o];
     if (k < 4) store_out<ACC>(a.dweight, c * 4 + k, total, a.dweight_bf16 != 0);
     else store_out<ACC>(a.dbias, c, total, a.dbias_bf16 != 0);
 }
@@ -433,7 +448,7 @@ cudaError_t launch_reduce_t(const BwdArgs& a, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     const int64_t n = a.plan.C * kPartialStride;
     cfg.gridDim = dim3((unsigned)((n + kRedOutputs - 1) / kRedOutputs));
-    cfg.blockDim = dim3(kRedOutputs * kRedSlices);
+    cfg.blockDim = dim3(kRedOutputs * red_slices(a.plan.rows));
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
