@@ -2,12 +2,13 @@
 
 The backward picks its launch shape on the host from the route: the wide shape
 (12 warps, up to 168 registers) for "bf16"-policy calls with a bias and longer
-documents, the deep shape (16 warps, at most 128 registers) otherwise. That rule
-rests on the compiled kernels: every wide-shape kernel and every forward kernel
-keeps its state in registers, and so do the deep shape's "bf16"-policy kernels
-without a bias. A source change that makes one of those spill silently makes
-its route slower, so this test compiles the kernels with ptxas' resource report
-and checks the spill counts. CPU only (nvcc cross-compiles for sm_103a).
+documents, the deep shape (16 warps, at most 128 registers) otherwise. That
+rule rests on the compiled kernels: every wide-shape kernel and every forward
+kernel (both batch shapes) keeps its state in registers, and so do the deep
+shape's "bf16"-policy kernels without a bias. A source change that makes one of
+those spill silently makes its route slower, so this test compiles the kernels
+with ptxas' resource report and checks the spill counts. CPU only (nvcc
+cross-compiles for sm_103a).
 """
 import concurrent.futures
 import os
@@ -70,7 +71,7 @@ def _main_kernels(bwd):
 def test_forward_kernels_do_not_spill(resources):
     fwd, _ = resources
     kernels = {n: r for n, r in fwd.items() if "fwd_kernel" in n}
-    assert len(kernels) == 6                      # weight dtype x bias kind
+    assert len(kernels) == 12                     # batch shape x weight dtype x bias kind
     for name, (regs, st, ld) in kernels.items():
         assert st == 0 and ld == 0, f"{name}: {regs} registers, spills {st}/{ld} bytes"
 

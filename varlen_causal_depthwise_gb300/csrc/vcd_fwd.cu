@@ -27,12 +27,6 @@
 namespace vcd {
 namespace {
 
-#ifndef VCD_FWD_U
-#define VCD_FWD_U 4
-#endif
-#ifndef VCD_FWD_NS
-#define VCD_FWD_NS 6
-#endif
 #ifndef VCD_FWD_PACKED
 #define VCD_FWD_PACKED 1
 #endif
@@ -41,19 +35,30 @@ namespace {
 #endif
 constexpr bool kPK = VCD_FWD_PACKED != 0;              // packed FP32x2 arithmetic (taps)
 constexpr bool kPKS = VCD_FWD_PACKED_SILU != 0;        // ... (SiLU)
-constexpr int kFwdU = VCD_FWD_U;                       // tokens per batch (even, <= 30)
-constexpr int kFwdNs = VCD_FWD_NS;                     // ring stages (>= 2)
 constexpr int kFwdColCh = 32 * kFwdVec;               // channels per unit column
 constexpr int kFwdRowBytes = 2 * kFwdColCh;            // bytes of a token's row segment
-constexpr int kFwdStageBytes = kFwdU * kFwdRowBytes;
-constexpr int kFwdWarpBytes = kFwdNs * kFwdStageBytes;
-constexpr int kFwdSmemBytes = kWarpsPerCta * kFwdWarpBytes;
-static_assert(kFwdU % 2 == 0 && kFwdU <= 30 && kFwdNs >= 2, "batch geometry");
+
+// Batch geometry of a forward shape (vcd_plan.h): tokens per batch and ring
+// stages.
+template <int SHAPE> struct FwdGeom;
+template <> struct FwdGeom<kFwdStream> { static constexpr int kU = 4, kNs = 6; };
+template <> struct FwdGeom<kFwdShortDocs> { static constexpr int kU = 8, kNs = 3; };
+template <int SHAPE> struct FwdShapeT : FwdGeom<SHAPE> {
+    using G = FwdGeom<SHAPE>;
+    static constexpr int kStageBytes = G::kU * kFwdRowBytes;
+    static constexpr int kWarpBytes = G::kNs * kStageBytes;
+    static constexpr int kSmemBytes = kWarpsPerCta * kWarpBytes;
+    static_assert(G::kU % 2 == 0 && G::kU <= 30 && G::kNs >= 2, "batch geometry");
+};
 
 __device__ __forceinline__ bool bit(uint32_t m, int i) { return (m >> i) & 1u; }
 
-template <bool W_BF16, int BIAS>
+template <int SHAPE, bool W_BF16, int BIAS>
 __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(const FwdArgs a) {
+    constexpr int kFwdU = FwdShapeT<SHAPE>::kU;                 // tokens per batch
+    constexpr int kFwdNs = FwdShapeT<SHAPE>::kNs;               // ring stages
+    constexpr int kFwdStageBytes = FwdShapeT<SHAPE>::kStageBytes;
+    constexpr int kFwdWarpBytes = FwdShapeT<SHAPE>::kWarpBytes;
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
     }
 }
 
-template <bool W_BF16, int BIAS>
+template <int SHAPE, bool W_BF16, int BIAS>
 int prepare_t() {
     // Once per (instantiation, device): allow the dynamic shared memory and
     // read the occupancy; both are host-side queries.
@@ -186,20 +191,21 @@ int prepare_t() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     if (occ[dev] > 0) return occ[dev];
-    if (cudaFuncSetAttribute(fwd_kernel<W_BF16, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kFwdSmemBytes) != cudaSuccess)
+    constexpr int kSmem = FwdShapeT<SHAPE>::kSmemBytes;
+    if (cudaFuncSetAttribute(fwd_kernel<SHAPE, W_BF16, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmem) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_kernel<W_BF16, BIAS>, kThreadsPerCta,
-                                                      kFwdSmemBytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_kernel<SHAPE, W_BF16, BIAS>, kThreadsPerCta,
+                                                      kSmem) != cudaSuccess)
         return 0;
     occ[dev] = n;
     return n;
 }
 
-template <bool W_BF16, int BIAS>
+template <int SHAPE, bool W_BF16, int BIAS>
 cudaError_t launch_fwd_t(const FwdArgs& a, int sm_count, cudaStream_t stream) {
-    const int occ = prepare_t<W_BF16, BIAS>();
+    const int occ = prepare_t<SHAPE, W_BF16, BIAS>();
     if (occ <= 0) return cudaErrorInvalidConfiguration;
     const int64_t ctas_needed = (a.plan.units + kWarpsPerCta - 1) / kWarpsPerCta;
     const int64_t resident = (int64_t)sm_count * occ;
@@ -207,19 +213,23 @@ cudaError_t launch_fwd_t(const FwdArgs& a, int sm_count, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
     cfg.blockDim = dim3(kThreadsPerCta);
-    cfg.dynamicSmemBytes = kFwdSmemBytes;
+    cfg.dynamicSmemBytes = FwdShapeT<SHAPE>::kSmemBytes;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, fwd_kernel<W_BF16, BIAS>, a);
+    return cudaLaunchKernelEx(&cfg, fwd_kernel<SHAPE, W_BF16, BIAS>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, int sm_count, cudaStream_t stream) {
     typedef cudaError_t (*L)(const FwdArgs&, int, cudaStream_t);
-    static const L launch[2][3] = {
-        {launch_fwd_t<false, kBiasNone>, launch_fwd_t<false, kBiasF32>, launch_fwd_t<false, kBiasBF16>},
-        {launch_fwd_t<true, kBiasNone>, launch_fwd_t<true, kBiasF32>, launch_fwd_t<true, kBiasBF16>}};
-    return launch[a.weight_bf16 ? 1 : 0][a.bias_kind](a, sm_count, stream);
+#define VCD_ROW(SH, WB) {launch_fwd_t<SH, WB, kBiasNone>, launch_fwd_t<SH, WB, kBiasF32>, \
+                         launch_fwd_t<SH, WB, kBiasBF16>}
+    // [shape][weight dtype][bias kind]
+    static const L launch[2][2][3] = {{VCD_ROW(kFwdStream, false), VCD_ROW(kFwdStream, true)},
+                                      {VCD_ROW(kFwdShortDocs, false), VCD_ROW(kFwdShortDocs, true)}};
+#undef VCD_ROW
+    const int shape = fwd_shape(a.plan.S, a.num_docs);
+    return launch[shape][a.weight_bf16 ? 1 : 0][a.bias_kind](a, sm_count, stream);
 }
 
 }  // namespace vcd

@@ -37,6 +37,13 @@ constexpr int kFwdCtasPerSm = VCD_FWD_CTAS_PER_SM;
 constexpr int64_t kGb300Sms = 152;
 constexpr int64_t kFwdTargetUnits = kGb300Sms * kFwdCtasPerSm * kWarpsPerCta;
 
+// Forward batch shapes: the same units and grid, different batches. Streaming
+// takes 4-token batches in a 6-stage ring; short documents (a start in most
+// batches, so each batch walks cu_seqlens and takes the masked path) take
+// 8-token batches in a 3-stage ring, which halves those per-batch costs. The
+// choice changes no result, only the time.
+enum FwdShape { kFwdStream = 0, kFwdShortDocs = 1 };
+
 // Backward launch shapes: one CTA per SM either way; they trade registers for
 // warps.
 //   kBwdWide: 12 warps, up to 168 registers a thread -- mask-free streaming
@@ -51,6 +58,11 @@ constexpr int kBwdShapeWarps[2] = {12, 16};
 // Mean document length (tokens) below which most batches hold a document
 // start and take the masked path.
 constexpr int64_t kShortDocTokens = 32;
+
+// The forward's batch shape for a call.
+inline int fwd_shape(int64_t S, int64_t num_docs) {
+    return num_docs * kShortDocTokens >= S ? kFwdShortDocs : kFwdStream;
+}
 
 // The backward's launch shape for a call: deep for the "fp32" policy and for
 // short documents (instruction-heavy paths, where more warps hide more
