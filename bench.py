@@ -49,7 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 # on; a changed kernel reports traffic null until it is profiled again. Taken on
 # the same workload at S = 16384 (a capture small enough for ncu's replay) and
 # scaled by the 4x units of S = 65536 (traffic is proportional to tokens).
-NCU_TRAFFIC = {"942f9b3647c4c491": 4 * 571.2e6}
+NCU_TRAFFIC = {"16674c7e7d3d58f1": 4 * 571.2e6}
 KERNEL_SOURCES = ["varlen_causal_depthwise_gb300/csrc/vcd_bwd.cu",
                   "varlen_causal_depthwise_gb300/csrc/vcd_device.cuh",
                   "varlen_causal_depthwise_gb300/csrc/vcd_plan.h"]
