@@ -71,7 +71,8 @@ def _main_kernels(bwd):
 def test_forward_kernels_do_not_spill(resources):
     fwd, _ = resources
     kernels = {n: r for n, r in fwd.items() if "fwd_kernel" in n}
-    assert len(kernels) == 12                     # batch shape x weight dtype x bias kind
+    # per batch shape: 4 routes specialised on their dtypes, 1 taking them at run time
+    assert len(kernels) == 10
     for name, (regs, st, ld) in kernels.items():
         assert st == 0 and ld == 0, f"{name}: {regs} registers, spills {st}/{ld} bytes"
 

@@ -53,6 +53,32 @@ template <int SHAPE> struct FwdShapeT : FwdGeom<SHAPE> {
 
 __device__ __forceinline__ bool bit(uint32_t m, int i) { return (m >> i) & 1u; }
 
+// The taps and the bias with their dtypes chosen at run time (one uniform
+// branch per unit), for the instantiation that serves routes by run-time
+// dtype.
+__device__ __forceinline__ void load_taps_rt(const void* weight, const void* bias, bool w_bf16,
+                                             int bias_kind, int64_t c0, bool active,
+                                             float2 (&w)[4][2], float2 (&b)[2]) {
+    if (w_bf16) {
+        if (bias_kind == kBiasF32) load_taps<true, kBiasF32, 2>(weight, bias, c0, active, w, b);
+        else if (bias_kind == kBiasBF16) load_taps<true, kBiasBF16, 2>(weight, bias, c0, active, w, b);
+        else load_taps<true, kBiasNone, 2>(weight, bias, c0, active, w, b);
+    } else {
+        if (bias_kind == kBiasF32) load_taps<false, kBiasF32, 2>(weight, bias, c0, active, w, b);
+        else if (bias_kind == kBiasBF16) load_taps<false, kBiasBF16, 2>(weight, bias, c0, active, w, b);
+        else load_taps<false, kBiasNone, 2>(weight, bias, c0, active, w, b);
+    }
+}
+
+// Routes by instantiation. The main loop is the same code for every route,
+// but the compiler schedules it differently per instantiation, and that moves
+// the time by up to 12% (measured on GB300): an instantiation specialised on
+// the dtypes is fastest for FP32 weights and for BF16 weights without a bias,
+// while BF16 weights with a bias run fastest through the one that takes the
+// dtypes at run time (65536 x 6144: 289 -> 260 us; 262144 x 8192: 1450 ->
+// 1342 us).
+constexpr int kRouteRuntime = -1;     // W_BF16 / BIAS template value: dtypes read at run time
+
 template <int SHAPE, bool W_BF16, int BIAS>
 __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(const FwdArgs a) {
     constexpr int kFwdU = FwdShapeT<SHAPE>::kU;                 // tokens per batch
@@ -85,7 +111,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
         const int nb = (n_rel + kFwdU - 1) / kFwdU;
 
         float2 w[4][2], b[2];
-        load_taps<W_BF16, BIAS, 2>(a.weight, a.bias, c0, active, w, b);
+        if (BIAS == kRouteRuntime)
+            load_taps_rt(a.weight, a.bias, a.weight_bf16 != 0, a.bias_kind, c0, active, w, b);
+        else
+            load_taps<W_BF16, BIAS, 2>(a.weight, a.bias, c0, active, w, b);
         DocCursor doc;
         doc.init(cu, ncu, (int)q0 - 2, lane);
         uint32_t carry = doc.starts(cu, ncu, (int)q0 - 2, 2, lane);            // bits of q0-2, q0-1
@@ -222,11 +251,12 @@ cudaError_t launch_fwd_t(const FwdArgs& a, int sm_count, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdArgs& a, int sm_count, cudaStream_t stream) {
     typedef cudaError_t (*L)(const FwdArgs&, int, cudaStream_t);
-#define VCD_ROW(SH, WB) {launch_fwd_t<SH, WB, kBiasNone>, launch_fwd_t<SH, WB, kBiasF32>, \
-                         launch_fwd_t<SH, WB, kBiasBF16>}
     // [shape][weight dtype][bias kind]
-    static const L launch[2][2][3] = {{VCD_ROW(kFwdStream, false), VCD_ROW(kFwdStream, true)},
-                                      {VCD_ROW(kFwdShortDocs, false), VCD_ROW(kFwdShortDocs, true)}};
+#define VCD_ROW(SH) {{launch_fwd_t<SH, false, kBiasNone>, launch_fwd_t<SH, false, kBiasF32>, \
+                      launch_fwd_t<SH, false, kBiasBF16>},                                      \
+                     {launch_fwd_t<SH, true, kBiasNone>, launch_fwd_t<SH, false, kRouteRuntime>,  \
+                      launch_fwd_t<SH, false, kRouteRuntime>}}
+    static const L launch[2][2][3] = {VCD_ROW(kFwdStream), VCD_ROW(kFwdShortDocs)};
 #undef VCD_ROW
     const int shape = fwd_shape(a.plan.S, a.num_docs);
     return launch[shape][a.weight_bf16 ? 1 : 0][a.bias_kind](a, sm_count, stream);
