@@ -46,20 +46,46 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ncu DRAM traffic (read + write bytes per launch) of the backward main kernel on
 # the default workload, keyed by the SHA-256 of the kernel sources it was taken
-# on; a changed kernel reports traffic null until it is profiled again. Taken on
-# the same workload at S = 16384 (a capture small enough for ncu's replay) and
-# scaled by the 4x units of S = 65536 (traffic is proportional to tokens).
-NCU_TRAFFIC = {"16674c7e7d3d58f1": 4 * 571.2e6}
+# on (comments and blank space stripped, so only code changes count); a changed
+# kernel reports traffic null until it is profiled again. Taken on the same
+# workload at S = 16384 (a capture small enough for ncu's replay) and scaled by
+# the 4x units of S = 65536 (traffic is proportional to tokens).
+NCU_TRAFFIC = {"cdc724d1fcca8f2f": 4 * 571.2e6}
 KERNEL_SOURCES = ["varlen_causal_depthwise_gb300/csrc/vcd_bwd.cu",
                   "varlen_causal_depthwise_gb300/csrc/vcd_device.cuh",
                   "varlen_causal_depthwise_gb300/csrc/vcd_plan.h"]
 
 
+def strip_comments(src):
+    """C/C++ source without comments and with blank space collapsed (string and
+    character literals kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            i = src.find("*/", i + 2)
+            i = n if i < 0 else i + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sha():
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -11,12 +11,14 @@
 //   db       sum_t dpre[t]
 //
 // Main kernel: one warp per work unit (32 * kBwdVec channels x L tokens,
-// vcd_plan.h),
-// walking its tokens forward once. x and dy stream through a per-warp
-// shared-memory ring (cp.async, kBwdNs - 1 batches of kBwdU tokens ahead). Registers
-// hold the x of the three previous tokens and their dpre, so each token gives
-// pre, dpre, its dweight / dbias products, and dx of the token three back in
-// gather form: dx[t-3] = w3 dpre[t-3] + w2 dpre[t-2] + w1 dpre[t-1] + w0 dpre[t].
+// vcd_plan.h), walking its tokens forward once, in one of two launch shapes
+// picked per call (one CTA of 12 warps per SM with up to 168 registers a
+// thread, or 16 warps with 128; BwdGeom below). x and dy stream through a
+// per-warp shared-memory ring (cp.async, kBwdNs - 1 batches of kBwdU tokens
+// ahead). Registers hold the x of the three previous tokens and their dpre,
+// so each token gives pre, dpre, its dweight / dbias products, and dx of the
+// token three back in gather form:
+//   dx[t-3] = w3 dpre[t-3] + w2 dpre[t-2] + w1 dpre[t-1] + w0 dpre[t].
 // A batch without a document start in positions q-2 .. q+U-1 (one bit mask
 // per batch from cu_seqlens) takes a mask-free path; otherwise each term is
 // predicated on "no document start in between". The unit reads x over
