@@ -80,11 +80,11 @@ def test_forward_kernels_do_not_spill(resources):
 def test_backward_shapes_fit_their_register_budgets(resources):
     _, bwd = resources
     k = _main_kernels(bwd)
-    # wide shape: "bf16" policy only, every weight dtype x bias kind x chunk form
+    # wide shape: "bf16" policy with a bias only, every weight dtype x bias dtype x chunk form
     wide = {key: r for key, r in k.items() if key[0] == 0}
     deep = {key: r for key, r in k.items() if key[0] == 1}
-    assert len(wide) == 12 and len(deep) == 24
-    assert all(key[3] == 0 for key in wide)
+    assert len(wide) == 8 and len(deep) == 24
+    assert all(key[3] == 0 and key[2] != 0 for key in wide)
     for key, (regs, st, ld) in wide.items():
         assert regs <= 168 and st == 0 and ld == 0, f"wide {key}: {regs} registers, spills {st}/{ld}"
     for key, (regs, st, ld) in deep.items():

@@ -96,6 +96,21 @@ def test_ragged_units(S, C, seed):
     full_check(wc, ("bf16", "fp32"), f"ragged S={S} C={C}")
 
 
+@pytest.mark.parametrize("wdt,bdt", [(torch.float32, None), (torch.float32, torch.float32),
+                                     (torch.float32, torch.bfloat16), (torch.bfloat16, None),
+                                     (torch.bfloat16, torch.float32), (torch.bfloat16, torch.bfloat16)])
+def test_short_documents_every_dtype_pair(wdt, bdt):
+    """Documents of 0-5 tokens (a start in almost every batch): the forward's
+    short-document batches and the backward's deep shape, for every weight /
+    bias dtype pair and both policies; ragged channel columns."""
+    rng = np.random.default_rng(77)
+    S = 900
+    lengths = synth.doc_lengths(("uniform", 0, 5, 0), S, rng)
+    assert len(lengths) * 32 >= S
+    wc = synth.custom(S, 136, lengths, seed=5, weight_dtype=wdt, bias_dtype=bdt)
+    full_check(wc, ("bf16", "fp32"), f"short docs {wdt} {bdt}")
+
+
 def test_no_bias_and_mixed_dtypes():
     for wdt, bdt in [(torch.float32, None), (torch.bfloat16, torch.float32),
                      (torch.float32, torch.bfloat16), (torch.bfloat16, None)]:

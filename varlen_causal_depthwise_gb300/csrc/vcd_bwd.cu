@@ -463,16 +463,19 @@ cudaError_t launch_bwd(const BwdArgs& a, int sm_count, cudaStream_t stream) {
     typedef cudaError_t (*L)(const BwdArgs&, int, cudaStream_t);
 #define VCD_ROW(SH, WB, POL) {launch_main_t<SH, WB, kBiasNone, POL>, launch_main_t<SH, WB, kBiasF32, POL>, \
                               launch_main_t<SH, WB, kBiasBF16, POL>}
-    // [weight dtype][bias kind]; the "fp32" policy runs the deep shape only
-    static const L wide_bf16[2][3] = {VCD_ROW(kBwdWide, false, kPolicyBF16), VCD_ROW(kBwdWide, true, kPolicyBF16)};
+    // [weight dtype][bias kind]. The wide shape serves "bf16"-policy calls with
+    // a bias only (bwd_shape), so it has no no-bias and no "fp32" kernels.
+    static const L wide_bf16[2][3] = {
+        {nullptr, launch_main_t<kBwdWide, false, kBiasF32, kPolicyBF16>, launch_main_t<kBwdWide, false, kBiasBF16, kPolicyBF16>},
+        {nullptr, launch_main_t<kBwdWide, true, kBiasF32, kPolicyBF16>, launch_main_t<kBwdWide, true, kBiasBF16, kPolicyBF16>}};
     static const L deep_bf16[2][3] = {VCD_ROW(kBwdDeep, false, kPolicyBF16), VCD_ROW(kBwdDeep, true, kPolicyBF16)};
     static const L deep_fp32[2][3] = {VCD_ROW(kBwdDeep, false, kPolicyFP32), VCD_ROW(kBwdDeep, true, kPolicyFP32)};
 #undef VCD_ROW
     const int wi = a.weight_bf16 ? 1 : 0;
     const bool fp32 = a.policy == kPolicyFP32;
-    if (fp32 && a.shape != kBwdDeep) return cudaErrorInvalidValue;
-    const L fn = fp32 ? deep_fp32[wi][a.bias_kind]
+    const L fn = fp32 ? (a.shape == kBwdDeep ? deep_fp32[wi][a.bias_kind] : nullptr)
                       : a.shape == kBwdWide ? wide_bf16[wi][a.bias_kind] : deep_bf16[wi][a.bias_kind];
+    if (fn == nullptr) return cudaErrorInvalidValue;     // a shape bwd_shape never picks
     cudaError_t e = fn(a, sm_count, stream);
     if (e != cudaSuccess) return e;
     return fp32 ? launch_reduce_t<double>(a, stream) : launch_reduce_t<float>(a, stream);
