@@ -111,6 +111,38 @@ def test_short_documents_every_dtype_pair(wdt, bdt):
     full_check(wc, ("bf16", "fp32"), f"short docs {wdt} {bdt}")
 
 
+@pytest.mark.parametrize("short_docs", [False, True])
+def test_parameter_dtypes_give_identical_bits(short_docs):
+    """BF16 and FP32 parameters run through different kernel instantiations
+    (and for the forward with a bias, one that reads the dtypes at run time);
+    with BF16-representable values and the same launch shape the arithmetic is
+    the same, so y, dx and FP32 dweight / dbias must match bit for bit."""
+    S, C = 1200, 264
+    if short_docs:
+        lengths = synth.doc_lengths(("uniform", 0, 5, 0), S, np.random.default_rng(8))
+    else:
+        lengths = [500, 0, 700]
+    base = synth.custom(S, C, lengths, seed=11).to(DEV)
+    Wv = base.weight.to(torch.bfloat16).float()
+    bv = base.bias.to(torch.bfloat16).float()
+    ref = None
+    for wdt in (torch.float32, torch.bfloat16):
+        for bdt in (torch.float32, torch.bfloat16):
+            W, b = Wv.to(wdt), bv.to(bdt)
+            y = vcd.conv1d_fwd(base.x, W, base.cu_seqlens, b)
+            outs = [y]
+            for pol in ("bf16", "fp32"):
+                dx, dW, dB = vcd.conv1d_bwd(base.x, base.dy, W, base.cu_seqlens, b, pol,
+                                            dweight=torch.empty(C, 4, device=DEV),
+                                            dbias=torch.empty(C, device=DEV))
+                outs += [dx, dW, dB]
+            torch.cuda.synchronize()
+            if ref is None:
+                ref = outs
+            for u, v in zip(outs, ref):
+                assert torch.equal(u, v), f"weight {wdt}, bias {bdt}"
+
+
 def test_no_bias_and_mixed_dtypes():
     for wdt, bdt in [(torch.float32, None), (torch.bfloat16, torch.float32),
                      (torch.float32, torch.bfloat16), (torch.bfloat16, None)]:

@@ -172,3 +172,23 @@ def test_malformed_cu_seqlens_rejected(lib):
     for cu in ([1, 4], [0, 3], [0, 3, 2, 4]):
         with pytest.raises(ValueError):
             oracle.fwd(x, W, torch.tensor(cu, dtype=torch.int32), None)
+
+
+def test_parameter_dtype_independence(lib):
+    """The weight and bias dtypes are storage only: with values that BF16
+    represents exactly, every (weight, bias) dtype pair gives the same y, dx,
+    dweight and dbias."""
+    w = _pins.small_case(40, 16, [15, 0, 25], seed=4)
+    Wv = w.weight.to(torch.bfloat16).float()          # BF16-representable values
+    bv = w.bias.to(torch.bfloat16).float()
+    ref = None
+    for wdt in (torch.float32, torch.bfloat16):
+        for bdt in (torch.float32, torch.bfloat16):
+            W, b = Wv.to(wdt), bv.to(bdt)
+            y, _ = oracle.fwd(w.x, W, w.cu_seqlens, b)
+            dx, _, dW, db = oracle.bwd(w.x, w.dy, W, w.cu_seqlens, b, "bf16")
+            out = (y, dx, dW, db)
+            if ref is None:
+                ref = out
+            for u, v in zip(out, ref):
+                np.testing.assert_array_equal(u, v)
