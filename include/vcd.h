@@ -70,14 +70,16 @@ int conv1d_fwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
  * as the forward query. */
 int conv1d_bwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
 
-/* Bytes of backward workspace one policy needs: the partial rows of the
+/* Bytes of backward workspace one policy needs (backward page, Parameters:
+ * workspace): the partial rows of the
  * "bf16" (policy 0) or "fp32" (policy 1) program for (S, C), the larger of
  * its two launch shapes; at most conv1d_bwd_workspace_size(S, C). Every
  * conv1d_bwd call of that policy accepts a workspace of this size. Errors as
  * the queries above, plus VCD_ERR_INVALID_ARG for an unknown policy. */
 int conv1d_bwd_route_workspace_size(int64_t S, int64_t C, int policy, size_t* bytes);
 
-/* Bytes of backward workspace one call needs, exactly: the partial rows that
+/* Bytes of backward workspace one call needs, exactly (backward page,
+ * Parameters: workspace): the partial rows that
  * conv1d_bwd writes and reads for these arguments (has_bias: a bias is
  * passed). The call picks one of two launch shapes from them -- 16 warps per
  * SM for the "fp32" policy, for documents shorter than 32 tokens on average
