@@ -435,6 +435,17 @@ def cpu_baseline(w, policy, tokens):
                       f"fwd + bwd ({policy}), single-threaded FP64 C"}
 
 
+def ref_tokens(args, C):
+    """Tokens per step of the reference arm: --ref-tokens, else 96 tokens cut
+    down (to 16 at least) so that --steps steps of the single-threaded FP64
+    oracle take about a minute (about 2.7 ms per token at C = 6144, in
+    proportion to C)."""
+    if args.ref_tokens is not None:
+        return args.ref_tokens
+    per_token_s = 2.7e-3 * C / 6144
+    return int(max(16, min(96, 60.0 / (max(args.steps, 1) * per_token_s))))
+
+
 def run_reference(args):
     ws, rank, local = dist_env()
     if rank != 0:
@@ -447,7 +458,7 @@ def run_reference(args):
     # inputs drawn on the GPU when there is one (faster; the oracle still runs on
     # the host cores), else on the CPU
     w = synth.make(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
-    x, dy, W, b, cu, n, _ = oracle_slice(w, args.ref_tokens)
+    x, dy, W, b, cu, n, _ = oracle_slice(w, ref_tokens(args, w.C))
     del w.x, w.dy
     for _ in range(args.warmup):
         oracle.fwd(x[:8], W, synth.cu_from_lengths([8]), b)
@@ -482,8 +493,9 @@ def main():
                     choices=["tiny", "mid", "linattn", "boundary", "large"])
     ap.add_argument("--cpu-tokens", type=int, default=4096,
                     help="tokens of the workload the CPU-baseline oracle leg processes")
-    ap.add_argument("--ref-tokens", type=int, default=96,
-                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--ref-tokens", type=int, default=None,
+                    help="tokens per step of the reference (oracle) arm (default: 96, fewer "
+                         "when --steps is large, so the arm's K steps take about a minute)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--S", type=int, default=None,
