@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 import torch
 
@@ -166,3 +167,29 @@ def test_binding_rejects_host_tensors_before_any_call():
         binding.conv1d_bwd(x, x, w, cu)
     with pytest.raises(ValueError, match="CUDA tensor"):
         binding.conv1d_bwd_noalloc(x, x, w, cu)
+
+
+def test_workspace_queries_are_consistent(lib):
+    """Random shapes: the per-call need is a whole number of 2560-byte partial
+    rows, never above its policy's need, which is never above the need of every
+    route; the policy's need is the larger of its launch shapes' needs (16 warps
+    for short documents or no bias, 12 warps with a bias), and the "fp32"
+    policy always takes the same shape."""
+    rng = np.random.default_rng(2024)
+    call = vcd.conv1d_bwd_call_workspace_size
+    for _ in range(300):
+        S = int(rng.integers(1, 1 << 22))
+        C = 8 * int(rng.integers(1, 1 << 13))
+        nd = int(rng.integers(1, S + 1))
+        total = vcd.conv1d_bwd_workspace_size(S, C)
+        for pol in ("bf16", "fp32"):
+            route = vcd.conv1d_bwd_route_workspace_size(S, C, pol)
+            assert route <= total
+            for hb in (True, False):
+                n = call(S, C, nd, pol, hb)
+                assert n % 2560 == 0 and 0 < n <= route
+            if pol == "fp32":
+                assert call(S, C, nd, pol, True) == call(S, C, 1, pol, False) == route
+            elif S > 32:
+                assert route == max(call(S, C, 1, pol, True), call(S, C, 1, pol, False))
+        assert total == max(vcd.conv1d_bwd_route_workspace_size(S, C, p) for p in ("bf16", "fp32"))
