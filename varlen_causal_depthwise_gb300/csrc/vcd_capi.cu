@@ -56,6 +56,34 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? VCD_OK : VCD_ERR_CUDA
 
 }  // namespace
 
+namespace vcd {
+
+// Every argument check of the backward except the workspace's, in conv1d_bwd's
+// order; the tensors themselves are checked only when S > 0 (an empty
+// sequence may pass NULL for them).
+int check_bwd_args(const void* x, const void* dy, int64_t S, int64_t C, const void* weight,
+                   int weight_dtype, const int32_t* cu_seqlens, int64_t num_docs, const void* bias,
+                   int bias_dtype, int policy, const void* dx, const void* dweight,
+                   int dweight_dtype, const void* dbias, int dbias_dtype) {
+    int st = check_shape(S, C, num_docs);
+    if (st != VCD_OK) return st;
+    if (policy != VCD_SILU_GRAD_BF16 && policy != VCD_SILU_GRAD_FP32) return VCD_ERR_INVALID_ARG;
+    if (!dtype_ok(weight_dtype) || (bias && !dtype_ok(bias_dtype))) return VCD_ERR_INVALID_ARG;
+    if (!dweight || !dtype_ok(dweight_dtype)) return VCD_ERR_INVALID_ARG;
+    if (dbias && (!bias || !dtype_ok(dbias_dtype))) return VCD_ERR_INVALID_ARG;  // dbias needs bias
+    const uintptr_t dwa = dweight_dtype == VCD_BF16 ? 2 : 4, dba = dbias_dtype == VCD_BF16 ? 2 : 4;
+    if (!aligned(dweight, dwa) || (dbias && !aligned(dbias, dba))) return VCD_ERR_MISALIGNED;
+    if (S == 0) return VCD_OK;
+    st = check_inputs(x, weight, weight_dtype, cu_seqlens, bias, bias_dtype);
+    if (st != VCD_OK) return st;
+    if (!dy || !dx) return VCD_ERR_INVALID_ARG;
+    if (!aligned(dy, 16) || !aligned(dx, 16)) return VCD_ERR_MISALIGNED;
+    if (dx == x || dx == dy) return VCD_ERR_INVALID_ARG;
+    return VCD_OK;
+}
+
+}  // namespace vcd
+
 extern "C" {
 
 int conv1d_fwd_workspace_size(int64_t S, int64_t C, size_t* bytes) {
@@ -120,25 +148,15 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* 
                int bias_dtype, int policy, void* dx, void* dweight, int dweight_dtype,
                void* dbias, int dbias_dtype, void* workspace, size_t workspace_bytes,
                cudaStream_t stream) {
-    int st = check_shape(S, C, num_docs);
+    int st = vcd::check_bwd_args(x, dy, S, C, weight, weight_dtype, cu_seqlens, num_docs, bias,
+                                 bias_dtype, policy, dx, dweight, dweight_dtype, dbias, dbias_dtype);
     if (st != VCD_OK) return st;
-    if (policy != VCD_SILU_GRAD_BF16 && policy != VCD_SILU_GRAD_FP32) return VCD_ERR_INVALID_ARG;
-    if (!dtype_ok(weight_dtype) || (bias && !dtype_ok(bias_dtype))) return VCD_ERR_INVALID_ARG;
-    if (!dweight || !dtype_ok(dweight_dtype)) return VCD_ERR_INVALID_ARG;
-    if (dbias && (!bias || !dtype_ok(dbias_dtype))) return VCD_ERR_INVALID_ARG;  // dbias needs bias
-    const uintptr_t dwa = dweight_dtype == VCD_BF16 ? 2 : 4, dba = dbias_dtype == VCD_BF16 ? 2 : 4;
-    if (!aligned(dweight, dwa) || (dbias && !aligned(dbias, dba))) return VCD_ERR_MISALIGNED;
-
     if (S == 0) {                                    // zero gradients, no kernel
+        const size_t dwa = dweight_dtype == VCD_BF16 ? 2 : 4, dba = dbias_dtype == VCD_BF16 ? 2 : 4;
         cudaError_t e = cudaMemsetAsync(dweight, 0, (size_t)C * 4 * dwa, stream);
         if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, (size_t)C * dba, stream);
         return cuda_status(e);
     }
-    st = check_inputs(x, weight, weight_dtype, cu_seqlens, bias, bias_dtype);
-    if (st != VCD_OK) return st;
-    if (!dy || !dx) return VCD_ERR_INVALID_ARG;
-    if (!aligned(dy, 16) || !aligned(dx, 16)) return VCD_ERR_MISALIGNED;
-    if (dx == x || dx == dy) return VCD_ERR_INVALID_ARG;
     const int weight_bf16 = weight_dtype == VCD_BF16;
     const int bias_kind = !bias ? vcd::kBiasNone : bias_dtype == VCD_BF16 ? vcd::kBiasBF16 : vcd::kBiasF32;
     const int shape = vcd::bwd_shape(S, num_docs, policy, bias != nullptr);

@@ -45,6 +45,12 @@ struct BwdArgs {
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, int sm_count, cudaStream_t stream);
+// conv1d_bwd's argument checks, all but the workspace's (vcd_capi.cu); a
+// vcd_status code.
+int check_bwd_args(const void* x, const void* dy, int64_t S, int64_t C, const void* weight,
+                   int weight_dtype, const int32_t* cu_seqlens, int64_t num_docs, const void* bias,
+                   int bias_dtype, int policy, const void* dx, const void* dweight,
+                   int dweight_dtype, const void* dbias, int dbias_dtype);
 // Main kernel, then the reduce kernel launched programmatically dependent on it.
 cudaError_t launch_bwd(const BwdArgs& a, int sm_count, cudaStream_t stream);
 

@@ -44,8 +44,14 @@ extern "C" int conv1d_bwd_noalloc(const void* x, const void* dy, int64_t S, int6
                                   int bias_dtype, int policy, void* dx, void* dweight,
                                   int dweight_dtype, void* dbias, int dbias_dtype,
                                   cudaStream_t stream) {
+    // The arguments first, as in conv1d_bwd: a bad call is refused before any
+    // CUDA call (the scratch lookup below) can fail on its own.
+    const int chk = vcd::check_bwd_args(x, dy, S, C, weight, weight_dtype, cu_seqlens, num_docs,
+                                        bias, bias_dtype, policy, dx, dweight, dweight_dtype,
+                                        dbias, dbias_dtype);
+    if (chk != VCD_OK) return chk;
     void* scratch = nullptr;
-    if (S > 0 && C > 0) {
+    if (S > 0) {
         if (vcd::bwd_workspace_bytes_for(S, C, policy) > (uint64_t)VCD_NOALLOC_SCRATCH_BYTES)
             return VCD_ERR_WORKSPACE_TOO_SMALL;   // shape needs more than the fixed scratch
         const int st = scratch_address(&scratch);
