@@ -31,6 +31,15 @@ MUTANTS = {
     "doc_start_strict": ("if ((int64_t)P->cu[mid] <= t) lo = mid; else hi = mid;",
                          "if ((int64_t)P->cu[mid] < t) lo = mid; else hi = mid;", 0),
     "weight_transposed": ("double term = P->w[c * 4 + k]", "double term = P->w[k * 4 + c % 4]", 0),
+    "bias_doubled": ("if (P->b) { nsum_add(&acc, P->b[c]);", "if (P->b) { nsum_add(&acc, 2.0 * P->b[c]);", 0),
+    "dpre_rounded_to_bf16": ("double d = g * silu_grad(p);",
+                             "double d = vcd_oracle_round_bf16(g * silu_grad(p));", 0),
+    "no_activation": ("double v = silu(pre);", "double v = pre;", 0),
+    "dx_from_dy": ("double d = dpre_at(P, j, c, policy, &a);", "double d = dy_at(P, j, c); a = 0.0;", 0),
+    "pre_tap_off_by_one": ("P->w[c * 4 + k] * xm(P, t, t - 3 + k, c)",
+                           "P->w[c * 4 + k] * xm(P, t, t - 2 + k, c)", 0),
+    "dweight_tap_off_by_one": ("double term = d * xm(P, t, t - 3 + k, c);",
+                               "double term = d * xm(P, t, t - 4 + k, c);", 0),
 }
 
 
