@@ -13,6 +13,11 @@ fails at least one of them:
                       cast and hand-placed midpoints.
 * ``pin_silu``        SiLU / SiLU' against torch FP64 and closed-form identities.
 * ``pin_golden``      a hand-worked example stored under tests/golden/.
+* ``pin_allowances``  the oracle's FP32-error allowances for y and dx against
+                      FP32 evaluations emulated in numpy in many evaluation
+                      orders (tests/_fp32_emul.py): never below an emulated
+                      error, and in aggregate at most ALLOW_RATIO_MAX times the
+                      largest emulated errors.
 
 They take the oracle library as an argument so the mutation test can run them
 against deliberately broken copies of the oracle.
@@ -27,6 +32,7 @@ import torch.nn.functional as F
 
 import oracle
 from varlen_causal_depthwise_gb300 import synth
+import _fp32_emul
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -246,3 +252,56 @@ def pin_golden(lib, name="hand_example.json"):
         want = sum(dpre[t] * xv[j] for t, j in g["dweight_pairs"][str(k)])
         assert abs(dW[0, k] - want) <= 1e-14 * max(1, abs(want)), (k, dW[0, k], want)
     assert abs(db[0] - dpre.sum()) <= 1e-14 * max(1, abs(dpre.sum()))
+
+
+# Summed over the elements of a case, the allowance may exceed the largest
+# error of the emulated FP32 evaluations by at most this factor. The oracle's
+# allowances sit at 26-42 on the cases below; any one of their constants made
+# 64 times larger moves its case to 93-2200.
+ALLOW_RATIO_MAX = 75.0
+
+_ALLOW_CASES = None
+
+
+def _allow_cases():
+    """Two problems of 8192 x 32 (long documents at sigma 1, documents of 0-5
+    tokens at sigma 2) with the emulated FP32 results, computed once."""
+    global _ALLOW_CASES
+    if _ALLOW_CASES is None:
+        cases = []
+        for seed, (docs, sigma) in enumerate([(("uniform", 1, 200, 2), 1.0),
+                                              (("uniform", 0, 5, 0), 2.0)]):
+            S, C = 8192, 32
+            lengths = synth.doc_lengths(docs, S, np.random.default_rng(seed))
+            w = synth.custom(S, C, lengths, seed=seed, x_sigma=sigma)
+            cu = w.cu_seqlens.numpy()
+            x, dy = w.x.float().numpy(), w.dy.float().numpy()
+            W, b = w.weight.float().numpy(), w.bias.float().numpy()
+            ys = _fp32_emul.forward_variants(x, W, b, cu)
+            dxs = {pol: _fp32_emul.backward_dx_variants(x, dy, W, b, cu, pol)
+                   for pol in ("bf16", "fp32")}
+            cases.append((w, ys, dxs))
+        _ALLOW_CASES = cases
+    return _ALLOW_CASES
+
+
+def _check_allowance(ref, allow, variants, what):
+    err = np.max([np.abs(v.astype(np.float64) - ref) for v in variants], axis=0)
+    bad = err > allow
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements where an FP32 evaluation is "
+                           f"further from the FP64 value than the allowance")
+    ratio = float(allow.sum() / err.sum())
+    assert ratio <= ALLOW_RATIO_MAX, f"{what}: allowance {ratio:.1f}x the FP32 errors seen"
+    return ratio
+
+
+def pin_allowances(lib):
+    """The y and dx allowances against emulated FP32 evaluations."""
+    ratios = {}
+    for i, (w, ys, dxs) in enumerate(_allow_cases()):
+        y, ya = oracle.fwd(w.x, w.weight, w.cu_seqlens, w.bias, lib=lib)
+        ratios[f"case{i} y"] = _check_allowance(y, ya, ys, f"case {i} y")
+        for pol in ("bf16", "fp32"):
+            dx, da, _, _ = oracle.bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, pol, lib=lib)
+            ratios[f"case{i} {pol} dx"] = _check_allowance(dx, da, dxs[pol], f"case {i} {pol} dx")
+    return ratios

@@ -19,7 +19,8 @@ from _check import bf16_close, grads_close
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-REPORT = {}
+REPORT = {}       # strict 1-ulp pass fractions
+REL_REPORT = {}   # rel-L2 of FP32 dweight / dbias
 
 
 def _np(t):
@@ -40,6 +41,33 @@ def run_bwd(w, policy, dweight_dtype=None, dbias_dtype=None, workspace=None):
                           dbias=dB, workspace=workspace)
 
 
+def run_grads(w, pol):
+    """The backward with FP32 gradient outputs, and -- when weight or bias is
+    BF16 -- a second call of the same route with the gradients in the
+    parameters' dtypes (the default of the pages' API). Returns
+    (dx, dW, dB, kw): kw holds the BF16 outputs for grads_close."""
+    dx, dW, dB = run_bwd(w, pol, torch.float32, torch.float32)
+    kw = {}
+    if w.weight.dtype == torch.bfloat16 or (w.bias is not None and w.bias.dtype == torch.bfloat16):
+        dx2, dW2, dB2 = run_bwd(w, pol)
+        torch.cuda.synchronize()
+        assert torch.equal(dx2, dx), "dx depends on the gradient output dtypes"
+        if dW2.dtype == torch.bfloat16:
+            kw["dw_bf16"] = dW2
+        if dB2 is not None and dB2.dtype == torch.bfloat16:
+            kw["db_bf16"] = dB2
+        del dx2
+    return dx, dW, dB, kw
+
+
+def check_grads(dW, dB, kw, rdw, rdb, pol, what, chans=None):
+    pick = (lambda t: _np(t)) if chans is None else (lambda t: _np(t)[chans])
+    bf = {k: pick(v) for k, v in kw.items()}
+    errs = grads_close(pick(dW), None if dB is None else pick(dB), rdw, rdb, pol, what, **bf)
+    for k, v in errs.items():
+        REL_REPORT[f"{what} {k}"] = v
+
+
 def full_check(wc, policies, what):
     """Every element against the full oracle; wc lives on the CPU."""
     w = wc.to(DEV)
@@ -48,16 +76,11 @@ def full_check(wc, policies, what):
     ry, ay = oracle.fwd(wc.x, wc.weight, wc.cu_seqlens, wc.bias)
     REPORT[f"{what} y strict"] = bf16_close(_np(y), ry, ay, f"{what} y")
     for pol in policies:
-        rdx, adx, rdw, rdb, mdw, mdb = oracle.bwd(wc.x, wc.dy, wc.weight, wc.cu_seqlens, wc.bias,
-                                                  pol, magnitudes=True)
-        # outputs in the parameters' dtypes (BF16 -> 1-ulp rule) and in FP32 (rel-L2)
-        for dwt in {w.weight.dtype, torch.float32}:
-            dx, dW, dB = run_bwd(w, pol, dwt, torch.float32 if dwt == torch.float32 else None)
-            torch.cuda.synchronize()
-            REPORT[f"{what} {pol} dx strict"] = bf16_close(_np(dx), rdx, adx, f"{what} {pol} dx")
-            bf_b = dB is not None and dB.dtype == torch.bfloat16
-            grads_close(_np(dW), None if dB is None else _np(dB), rdw, rdb, pol,
-                        dW.dtype == torch.bfloat16, bf_b, f"{what} {pol}", mdw, mdb, wc.S)
+        rdx, adx, rdw, rdb = oracle.bwd(wc.x, wc.dy, wc.weight, wc.cu_seqlens, wc.bias, pol)
+        dx, dW, dB, kw = run_grads(w, pol)
+        torch.cuda.synchronize()
+        REPORT[f"{what} {pol} dx strict"] = bf16_close(_np(dx), rdx, adx, f"{what} {pol} dx")
+        check_grads(dW, dB, kw, rdw, rdb, pol, f"{what} {pol}")
 
 
 # ------------------------------------------------------------- small, full --
@@ -201,21 +224,15 @@ def test_recipes_full_size_sampled(name):
     del y
     chans = sample_channels(w.C, rng)
     for pol in synth.RECIPES[name].policies:
-        for dwt in {w.weight.dtype, torch.float32}:
-            dx, dW, dB = run_bwd(w, pol, dwt, torch.float32 if dwt == torch.float32 else None)
-            torch.cuda.synchronize()
-            rdx, adx = oracle.bwd_dx_at(xc, dyc, wgt, cu, ts, cs, bias, pol)
-            dxg = dx[torch.from_numpy(ts).to(DEV), torch.from_numpy(cs).to(DEV)]
-            REPORT[f"{name} full {pol} dx strict"] = bf16_close(_np(dxg), rdx, adx,
-                                                                f"{name} {pol} dx")
-            del dx
-            rdw, rdb, mdw, mdb = oracle.bwd_params_at(xc, dyc, wgt, cu, chans, bias, pol,
-                                                      magnitudes=True)
-            gdw = _np(dW)[chans]
-            gdb = None if dB is None else _np(dB)[chans]
-            grads_close(gdw, gdb, rdw, rdb, pol, dW.dtype == torch.bfloat16,
-                        dB is not None and dB.dtype == torch.bfloat16, f"{name} {pol}", mdw, mdb,
-                        w.S)
+        dx, dW, dB, kw = run_grads(w, pol)
+        torch.cuda.synchronize()
+        rdx, adx = oracle.bwd_dx_at(xc, dyc, wgt, cu, ts, cs, bias, pol)
+        dxg = dx[torch.from_numpy(ts).to(DEV), torch.from_numpy(cs).to(DEV)]
+        REPORT[f"{name} full {pol} dx strict"] = bf16_close(_np(dxg), rdx, adx,
+                                                            f"{name} {pol} dx")
+        del dx
+        rdw, rdb = oracle.bwd_params_at(xc, dyc, wgt, cu, chans, bias, pol)
+        check_grads(dW, dB, kw, rdw, rdb, pol, f"{name} full {pol}", chans)
     del w
     torch.cuda.empty_cache()
 
@@ -391,14 +408,6 @@ def test_native_library_is_loaded():
     assert os.path.realpath(vcd.library_path()) in maps
 
 
-def test_report_strict_fractions(capsys):
-    """Prints the strict 1-ulp pass fractions gathered above (informational)."""
-    with capsys.disabled():
-        for k, v in sorted(REPORT.items()):
-            if v < 1.0:
-                print(f"  strict-1ulp {k}: {v:.6f}")
-
-
 @pytest.mark.parametrize("cu", [[0, 50, 20, 100], [0, 30, 60], [0, -5, 1000000, 100],
                                 [10, 50, 100], [0, 100, 100, 7, 100]])
 def test_malformed_cu_seqlens_is_memory_safe(cu):
@@ -444,3 +453,17 @@ def test_random_shapes_documents_dtypes(seed):
     wc = synth.custom(S, C, lengths, seed=seed, x_sigma=float(rng.choice([0.5, 1.0, 3.0])),
                       weight_dtype=wdt, bias_dtype=bdt)
     full_check(wc, ("bf16", "fp32"), f"random seed={seed} S={S} C={C}")
+
+
+def test_report_accuracy(capsys):
+    """Prints the strict 1-ulp pass fractions below 1 and the rel-L2 errors of
+    the FP32 gradients gathered above, beside the backward page's figures
+    (about 3e-5 under "bf16", 2e-7 under "fp32"). Each was asserted where it
+    was measured."""
+    with capsys.disabled():
+        for k, v in sorted(REPORT.items()):
+            if v < 1.0:
+                print(f"  strict-1ulp {k}: {v:.6f}")
+        for k, v in sorted(REL_REPORT.items()):
+            if " full " in k:
+                print(f"  rel-L2 {k}: {v:.3g}")

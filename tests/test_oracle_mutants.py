@@ -40,6 +40,24 @@ MUTANTS = {
                            "P->w[c * 4 + k] * xm(P, t, t - 2 + k, c)", 0),
     "dweight_tap_off_by_one": ("double term = d * xm(P, t, t - 3 + k, c);",
                                "double term = d * xm(P, t, t - 4 + k, c);", 0),
+    # allowances made 64 times too generous (each would hide GPU errors) ...
+    "allow_pre_x64": ("return 10.0 * U32 * mag;", "return 640.0 * U32 * mag;", 0),
+    "allow_fwd_pre_carry_x64": ("*allow = 1.1 * pre_allow(mag)", "*allow = 70.0 * pre_allow(mag)", 0),
+    "allow_silu_x64": ("(16.0 + 2.0 * fabs(pre)) * U32 * fabs(v)",
+                       "(1024.0 + 128.0 * fabs(pre)) * U32 * fabs(v)", 0),
+    "allow_silu_grad_x64": ("double e_grad = (16.0 + 2.0 * fabs(p)) * U32",
+                            "double e_grad = (1024.0 + 128.0 * fabs(p)) * U32", 0),
+    "allow_dpre_product_x64": ("2.0 * U32 * fabs(d);", "128.0 * U32 * fabs(d);", 0),
+    "allow_fp32_policy_dgrad_x64": ("*dgrad = 0.5 * e_pre;", "*dgrad = 32.0 * e_pre;", 0),
+    "allow_midpoint_window_x64": ("double lo = vcd_oracle_round_bf16(pre - e_pre);",
+                                  "double lo = vcd_oracle_round_bf16(pre - 64.0 * e_pre);", 0),
+    "allow_dx_carry_x64": ("e += fabs(wk) * a;", "e += 64.0 * fabs(wk) * a;", 0),
+    "allow_dx_sum_x64": ("*allow = e + 8.0 * U32 * mag;", "*allow = e + 512.0 * U32 * mag;", 0),
+    # ... and too tight (GPU-correct values would be refused)
+    "allow_pre_too_small": ("return 10.0 * U32 * mag;", "return 0.01 * U32 * mag;", 0),
+    "allow_midpoint_neighbours_dropped": ("*dgrad = d;", "*dgrad = 0.0;", 0),
+    "allow_silu_grad_dropped": ("double e_grad = (16.0 + 2.0 * fabs(p)) * U32",
+                                "double e_grad = 0.0 * U32", 0),
 }
 
 
@@ -59,6 +77,7 @@ def _battery(lib):
     for seed in range(2):
         _pins.pin_conv1d(lib, seed)
     _pins.pin_fd(lib, 0)
+    _pins.pin_allowances(lib)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

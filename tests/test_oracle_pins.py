@@ -157,6 +157,13 @@ def test_sampled_entry_points_match_full(lib):
         np.testing.assert_array_equal(dbs, db[chans])
 
 
+def test_allowances_against_fp32_evaluations(lib):
+    """Every emulated FP32 evaluation of y and dx lies within the oracle's
+    allowance, and the allowance is not inflated far past those errors."""
+    ratios = _pins.pin_allowances(lib)
+    assert min(ratios.values()) >= 1.0, ratios
+
+
 def test_allowance_is_small_where_well_conditioned(lib):
     """The FP32 allowance stays far below a BF16 ulp except near cancellation."""
     w = synth.make("tiny", S=256, C=32)
