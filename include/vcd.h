@@ -163,9 +163,13 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C,
  * that loads the library holds until the process exits.
  *   - Shapes whose partial rows exceed VCD_NOALLOC_SCRATCH_BYTES are refused
  *     with VCD_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
- *   - The first call on a device (with S > 0) looks up the array's device
- *     address on that device (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture.
+ *   - A call with S > 0 made outside stream capture looks up the array's
+ *     device address on the current device (cudaGetSymbolAddress, a host-side
+ *     query) and remembers it for that device; a call made while `stream` is
+ *     capturing uses the remembered address. Make one call on a device before
+ *     capturing calls on it: a first call made during capture runs that lookup
+ *     (and the kernels' one-time set-up: shared-memory attribute and occupancy
+ *     queries) inside the capture.
  *   - Every call shares the one array. It needs no clearing (each call writes
  *     all the rows it reads), but two calls whose kernels may overlap on the
  *     GPU -- different streams, no ordering between them -- race on it and

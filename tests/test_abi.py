@@ -193,3 +193,27 @@ def test_workspace_queries_are_consistent(lib):
             elif S > 32:
                 assert route == max(call(S, C, 1, pol, True), call(S, C, 1, pol, False))
         assert total == max(vcd.conv1d_bwd_route_workspace_size(S, C, p) for p in ("bf16", "fp32"))
+
+
+NOALLOC_BYTES = 8 << 20      # VCD_NOALLOC_SCRATCH_BYTES in include/vcd.h
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+VCD_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == NOALLOC_BYTES
+
+
+@pytest.mark.parametrize("S,C,policy,fits", [
+    (17408, 6144, "fp32", True),        # ceil(S/256) * 48 columns = 3264 rows <= 3276
+    (17664, 6144, "fp32", False),       # 69 * 48 = 3312 rows
+    (1 << 20, 419328, "bf16", True),    # 3276 columns of one row each
+    (1 << 20, 419336, "bf16", False),   # 3277 columns
+    (262144, 311296, "bf16", True),
+])
+def test_noalloc_limits_stated_in_the_header(lib, S, C, policy, fits):
+    """The shapes include/vcd.h names on either side of the fixed scratch's
+    limit: the policy's largest need (the size conv1d_bwd_noalloc checks)
+    against VCD_NOALLOC_SCRATCH_BYTES."""
+    need = vcd.conv1d_bwd_route_workspace_size(S, C, policy)
+    assert (need <= NOALLOC_BYTES) == fits, (S, C, policy, need)

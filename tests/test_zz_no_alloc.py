@@ -70,3 +70,54 @@ def test_noalloc_refuses_shapes_beyond_its_scratch():
     assert _abi_noalloc(w, "bf16", dx, dW, dB) == binding.VCD_ERR_WORKSPACE_TOO_SMALL
     with pytest.raises(vcd.VcdError, match="workspace"):
         vcd.conv1d_bwd_noalloc(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, "bf16")
+
+
+def test_noalloc_fp32_policy_at_its_stated_limit():
+    """S = 17408 at C = 6144: the largest "fp32"-policy shape the header says
+    fits the fixed scratch (3264 of its 3276 rows)."""
+    S, C = 17408, 6144
+    w = synth.make("linattn", device=DEV, S=S, C=C)
+    ref = vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, "fp32",
+                         dweight=torch.empty(C, 4, device=DEV), dbias=torch.empty(C, device=DEV))
+    for _ in range(2):
+        dx = torch.full_like(w.x, float("nan"))
+        dW = torch.full((C, 4), float("nan"), device=DEV)
+        dB = torch.full((C,), float("nan"), device=DEV)
+        assert _abi_noalloc(w, "fp32", dx, dW, dB) == binding.VCD_OK
+        torch.cuda.synchronize()
+        assert torch.equal(dx, ref[0]) and torch.equal(dW, ref[1]) and torch.equal(dB, ref[2])
+
+
+def test_noalloc_empty_sequence_gives_zero_gradients():
+    w = synth.custom(0, 64, [0, 0], seed=0).to(DEV)
+    dx = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    dW = torch.ones(64, 4, device=DEV)
+    dB = torch.ones(64, device=DEV)
+    assert _abi_noalloc(w, "bf16", dx, dW, dB) == binding.VCD_OK
+    torch.cuda.synchronize()
+    assert not dW.any() and not dB.any()
+
+
+def test_noalloc_captured_after_a_first_call_replays_the_same_bits():
+    """The supported order: one call outside capture on the device, then calls
+    captured into a CUDA graph; every replay gives the eager call's bits."""
+    w = synth.make("boundary", device=DEV, S=4096, C=1032)
+    C = w.C
+    eager = [torch.empty_like(w.x), torch.empty(C, 4, device=DEV), torch.empty(C, device=DEV)]
+    assert _abi_noalloc(w, "bf16", *eager) == binding.VCD_OK
+    torch.cuda.synchronize()
+    out = [torch.zeros_like(t) for t in eager]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            assert _abi_noalloc(w, "bf16", *out) == binding.VCD_OK
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for t in out:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(eager, out):
+            assert torch.equal(a, b)

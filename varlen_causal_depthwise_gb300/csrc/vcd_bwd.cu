@@ -31,6 +31,8 @@
 // griddepcontrol for the main kernel and sums the partial rows of each channel
 // in a fixed order (FP32, or FP64 under the "fp32" policy), so the gradients
 // are bitwise reproducible for a given (S, C) and route.
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -402,12 +404,14 @@ __global__ void __launch_bounds__(kRedOutputs * kRedMaxSlices, 4) bwd_reduce_ker
 template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG>
 int prepare_main_t() {
     // Once per (instantiation, device): allow the dynamic shared memory and
-    // read the occupancy; both are host-side queries.
+    // read the occupancy; both are host-side queries. The cache entries are
+    // atomic (host threads may get here at once; each stores the same value).
     using SH = BwdShapeT<SHAPE>;
-    static int occ[kMaxDevices] = {0};
+    static std::atomic<int> occ[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-    if (occ[dev] > 0) return occ[dev];
+    const int known = occ[dev].load(std::memory_order_relaxed);
+    if (known > 0) return known;
     if (cudaFuncSetAttribute(bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, SH::kSmemBytes) != cudaSuccess)
         return 0;
@@ -415,7 +419,7 @@ int prepare_main_t() {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>,
                                                       SH::kThreads, SH::kSmemBytes) != cudaSuccess)
         return 0;
-    occ[dev] = n;
+    occ[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -1,6 +1,8 @@
 // vcd_capi.cu -- the extern "C" entry points declared in include/vcd.h:
 // argument checks, the S == 0 cases, the work-unit plan, and the launches.
 // Nothing here allocates, synchronizes or reads device memory on the host.
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -10,20 +12,24 @@
 
 namespace {
 
-
-// SM count of the current device (cached; a host-side attribute query).
+// SM count of the current device (cached; a host-side attribute query). Host
+// threads may make their first calls at once: the cache entries are atomic,
+// and filling one twice stores the same value.
 int sm_count_of_current(int* sms) {
-    static int cache[vcd::kMaxDevices] = {0};
+    static std::atomic<int> cache[vcd::kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return VCD_ERR_CUDA;
-    if (dev >= 0 && dev < vcd::kMaxDevices && cache[dev] > 0) {
-        *sms = cache[dev];
-        return VCD_OK;
+    if (dev >= 0 && dev < vcd::kMaxDevices) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *sms = c;
+            return VCD_OK;
+        }
     }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         return VCD_ERR_CUDA;
-    if (dev >= 0 && dev < vcd::kMaxDevices) cache[dev] = n;
+    if (dev >= 0 && dev < vcd::kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
     *sms = n;
     return VCD_OK;
 }

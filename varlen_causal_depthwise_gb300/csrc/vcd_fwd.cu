@@ -17,6 +17,8 @@
 // token's result does not depend on where batches fall.
 //
 // Memory-bound: 4 bytes of HBM traffic per element (read x, write y).
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -215,11 +217,13 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
 template <int SHAPE, bool W_BF16, int BIAS>
 int prepare_t() {
     // Once per (instantiation, device): allow the dynamic shared memory and
-    // read the occupancy; both are host-side queries.
-    static int occ[kMaxDevices] = {0};
+    // read the occupancy; both are host-side queries. The cache entries are
+    // atomic (host threads may get here at once; each stores the same value).
+    static std::atomic<int> occ[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-    if (occ[dev] > 0) return occ[dev];
+    const int known = occ[dev].load(std::memory_order_relaxed);
+    if (known > 0) return known;
     constexpr int kSmem = FwdShapeT<SHAPE>::kSmemBytes;
     if (cudaFuncSetAttribute(fwd_kernel<SHAPE, W_BF16, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmem) != cudaSuccess)
@@ -228,7 +232,7 @@ int prepare_t() {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_kernel<SHAPE, W_BF16, BIAS>, kThreadsPerCta,
                                                       kSmem) != cudaSuccess)
         return 0;
-    occ[dev] = n;
+    occ[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

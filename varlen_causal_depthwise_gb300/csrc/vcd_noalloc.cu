@@ -5,8 +5,11 @@
 // The array is a file-scope __device__ variable: every GPU on which the
 // library is loaded holds VCD_NOALLOC_SCRATCH_BYTES of it until the process
 // exits. In host code its name is only a host-side stand-in, so the device
-// address is looked up once per device with cudaGetSymbolAddress (on the first
-// call made with that device current) and cached.
+// address comes from cudaGetSymbolAddress with the device current. A call
+// made outside stream capture looks it up afresh (a host-side query), so a
+// device reset, after which the array may live at another address, is
+// followed; a call made while its stream is capturing uses the address the
+// last call outside capture found on that device.
 #include <atomic>
 
 #include <cuda_runtime.h>
@@ -22,14 +25,19 @@ static __device__ __align__(256) unsigned char g_bwd_scratch[VCD_NOALLOC_SCRATCH
 
 std::atomic<void*> g_scratch_addr[vcd::kMaxDevices];
 
-// Device address of g_bwd_scratch on the current device (looked up once).
-int scratch_address(void** out) {
+// Device address of g_bwd_scratch on the current device.
+int scratch_address(cudaStream_t stream, void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= vcd::kMaxDevices) return VCD_ERR_CUDA;
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return VCD_ERR_CUDA;
+    void* p = cap == cudaStreamCaptureStatusNone
+                  ? nullptr : g_scratch_addr[dev].load(std::memory_order_acquire);
     if (p == nullptr) {
-        if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr)
+        if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) {
+            g_scratch_addr[dev].store(nullptr, std::memory_order_release);
             return VCD_ERR_CUDA;
+        }
         g_scratch_addr[dev].store(p, std::memory_order_release);
     }
     *out = p;
@@ -54,7 +62,7 @@ extern "C" int conv1d_bwd_noalloc(const void* x, const void* dy, int64_t S, int6
     if (S > 0) {
         if (vcd::bwd_workspace_bytes_for(S, C, policy) > (uint64_t)VCD_NOALLOC_SCRATCH_BYTES)
             return VCD_ERR_WORKSPACE_TOO_SMALL;   // shape needs more than the fixed scratch
-        const int st = scratch_address(&scratch);
+        const int st = scratch_address(stream, &scratch);
         if (st != VCD_OK) return st;
     }
     // The partial rows are written in full before the reduce reads them, so
