@@ -18,9 +18,16 @@ Printed JSON (one line, rank 0):
                host->device copies of the step's inputs and device->host copies
                of its outputs inside the timed region.
   roofline     backward call (its main kernel dominates the step) against the
-               measured HBM copy bandwidth.
+               measured HBM copy bandwidth, and against the library's own
+               streaming kernel moving the same bytes (ceiling_gbs).
+  ceiling      vcd_stream_copy (include/vcd_stream.h) timed on the workload's
+               own buffers: the forward's traffic (read x, write y) and the
+               backward's (read x and dy, write dx) with no arithmetic.
+  routes       every workload and SiLU' policy the operation is specified on,
+               forward and backward timed the same way (--no-sweep skips it).
   cpu_baseline the FP64 oracle (test infrastructure, single-threaded C) timed on
-               a bounded slice of the same workload.
+               a bounded slice of the same workload, and the same slice split
+               by channels over every host core.
 
 Multi-GPU (torchrun, N > 1): every rank runs an independent replica on its own
 GPU (the operation has no exchange step); value sums the ranks' bytes over the
@@ -113,6 +120,7 @@ class ClockSampler:
         self.window = (t0, t1)
 
     def __enter__(self):
+        self.nvml = NvmlSampler(self.gpu).__enter__()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
@@ -123,6 +131,7 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
+        self.nvml.__exit__()
         self.out = ""
         if self.proc is not None:
             self.proc.terminate()
@@ -152,10 +161,78 @@ class ClockSampler:
             for n, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
+        n_smi = len(sm)
+        if self.window:
+            nsm, nreasons = self.nvml.in_window(*self.window)
+            sm += nsm
+            reasons |= nreasons
+            if self.nvml.max_mhz:
+                mx.append(self.nvml.max_mhz)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "samples_nvidia_smi": n_smi,
+                "samples_nvml": len(sm) - n_smi}
+
+
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (ctypes, read-only
+    queries) every ~2 ms on a host thread, so that a timed region of a few
+    milliseconds still gets several samples. Silently empty where NVML is
+    missing; the nvidia-smi sampler runs beside it."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, gpu_index, period_s=0.002):
+        self.gpu, self.period = gpu_index, period_s
+        self.samples, self.max_mhz = [], None
+        self._stop = None
+
+    def __enter__(self):
+        import ctypes
+        import threading
+
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return self
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+                return self
+            reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except (OSError, AttributeError):
+            return self
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self._nv, self._stop = nv, threading.Event()
+
+        def poll():
+            clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+            while not self._stop.is_set():
+                if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                        reasons(h, ctypes.byref(rs)) == 0:
+                    self.samples.append((time.time(), float(clk.value), int(rs.value)))
+                self._stop.wait(self.period)
+
+        self._thread = threading.Thread(target=poll, daemon=True)
+        self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._stop is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+            self._nv.nvmlShutdown()
+
+    def in_window(self, t0, t1):
+        sm, reasons = [], set()
+        for ts, clk, rs in self.samples:
+            if t0 <= ts <= t1:
+                sm.append(clk)
+                reasons.update(n for bit, n in self.REASONS.items() if rs & bit)
+        return sm, reasons
 
 
 def dist_env():
@@ -252,13 +329,103 @@ def run_ours(args):
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
     total_ms = reduce_max(total_ms, dev)
+    extra = {"ceiling": ceiling_leg(w, y, dx, stream, 20)}
+    if not args.no_sweep and rank == 0:
+        extra["routes"] = sweep_leg(dev, 20, measured_peak()[0])
 
     # ---- end to end: pinned host buffers through the public API ----
     if args.no_e2e:
-        return finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, None, ws, rank)
+        return finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, None, ws, rank,
+                      extra)
     e2e = e2e_pipelined(w, policy, K, dev, vcd)
     e2e = (reduce_max(e2e[0], dev),) + e2e[1:]
-    return finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws, rank)
+    return finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws, rank,
+                  extra)
+
+
+def time_events(fn, iters, stream, flush=None):
+    """Median device time (us) of fn() over iters runs, CUDA events on `stream`;
+    flush() (not timed) runs before each when given."""
+    out = []
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        out.append((a, b))
+    torch.cuda.synchronize()
+    return 1e3 * statistics.median(a.elapsed_time(b) for a, b in out)
+
+
+def ceiling_leg(w, y, dx, stream, iters):
+    """The library's streaming kernel over the workload's own buffers: the
+    forward's traffic (x -> y) and the backward's (x, dy -> dx), each at the
+    best of 1, 2 and 4 CTAs of 512 threads per SM."""
+    from varlen_causal_depthwise_gb300 import binding
+
+    E = w.x.numel()
+    res = {}
+    for leg, args, nbytes in (("fwd_mix", (w.x, y, None), 4 * E),
+                              ("bwd_mix", (w.x, dx, w.dy), 6 * E)):
+        best = None
+        for bps in (1, 2, 4):
+            fn = lambda: binding.stream_copy(args[0], args[1], args[2], bps, stream)
+            for _ in range(3):
+                fn()
+            us = time_events(fn, iters, stream)
+            if best is None or us < best[0]:
+                best = (us, bps)
+        res[leg] = {"us_median": round(best[0], 2), "blocks_per_sm": best[1], "bytes": nbytes,
+                    "gbs": round(nbytes / (best[0] * 1e-6) / 1e9, 1)}
+    return res
+
+
+def sweep_leg(dev, iters, peak):
+    """Forward and backward of every specified workload and policy, timed on
+    their own inputs; workloads whose tensors fit in L2 several times over are
+    timed with L2 flushed before each call."""
+    import varlen_causal_depthwise_gb300 as vcd
+    from varlen_causal_depthwise_gb300 import synth
+
+    stream = torch.cuda.current_stream(dev)
+    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = lambda: scrub.fill_(1)
+    out = {}
+    for name, recipe in synth.RECIPES.items():
+        w = synth.make(name, device=dev)
+        S, C = w.S, w.C
+        small = 2 * S * C < 4 * (128 << 20)
+        y = torch.empty_like(w.x)
+        dx = torch.empty_like(w.x)
+        ws = torch.empty(vcd.conv1d_bwd_workspace_size(S, C), dtype=torch.uint8, device=dev)
+        dW = torch.empty(C, 4, dtype=w.weight.dtype, device=dev)
+        dB = None if w.bias is None else torch.empty(C, dtype=w.bias.dtype, device=dev)
+        fwd = lambda: vcd.conv1d_fwd(w.x, w.weight, w.cu_seqlens, w.bias, y=y, stream=stream)
+        for _ in range(3):
+            fwd()
+        f_us = time_events(fwd, iters, stream, flush if small else None)
+        fwd_b = 4 * S * C
+        for pol in recipe.policies:
+            bwd = lambda: vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, pol, dx=dx,
+                                         dweight=dW, dbias=dB, workspace=ws, stream=stream)
+            for _ in range(3):
+                bwd()
+            b_us = time_events(bwd, iters, stream, flush if small else None)
+            bwd_b = compulsory_bytes(S, C, vcd_call_bytes(w, pol))[1]
+            row = {"S": S, "C": C, "docs": w.num_docs, "policy": pol,
+                   "l2": "flushed before each call" if small else "inputs larger than L2"}
+            for d, us, nb in (("fwd", f_us, fwd_b), ("bwd", b_us, bwd_b)):
+                gbs = nb / (us * 1e-6) / 1e9
+                row[d] = {"us_median": round(us, 2), "gbs": round(gbs, 1),
+                          "frac_of_measured": round(gbs / peak, 4),
+                          "frac_of_8tbs_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+                          "mtokens_per_s": round(S / (us * 1e-6) / 1e6, 2)}
+            out[f"{name}/{pol}"] = row
+        del w, y, dx, ws
+        torch.cuda.empty_cache()
+    return out
 
 
 def e2e_pipelined(w, policy, K, dev, vcd):
@@ -328,7 +495,7 @@ def e2e_pipelined(w, policy, K, dev, vcd):
     return e0.elapsed_time(e1) / Ke, h2d, d2h
 
 
-def finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws, rank):
+def finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws, rank, extra):
     import torch.distributed as dist
 
     # the partial rows this call writes and reads back (the workspace size
@@ -342,10 +509,13 @@ def finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws
     bwd_mean_us = 1e3 * statistics.mean(bwd_ms)
     clocks = clk.summary()
 
-    def direction(nbytes, us):
+    ceil = extra["ceiling"]
+
+    def direction(nbytes, us, mix):
         gbs = nbytes / (us * 1e-6) / 1e9
         return {"us_median": round(us, 2), "gbs": round(gbs, 1),
                 "frac_of_measured": round(gbs / peak, 4),
+                "frac_of_own_ceiling": round(gbs / ceil[mix]["gbs"], 4),
                 "frac_of_8tbs_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
                 "mtokens_per_s": round(S / (us * 1e-6) / 1e6, 2),
                 "bytes": nbytes}
@@ -374,7 +544,8 @@ def finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws
                    "S": S, "C": C, "num_docs": w.num_docs, "policy": policy,
                    "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (no flush needed)"},
-        "detail": {"fwd": direction(fwd_b, fwd_us), "bwd": direction(bwd_b, bwd_us),
+        "detail": {"fwd": direction(fwd_b, fwd_us, "fwd_mix"),
+                   "bwd": direction(bwd_b, bwd_us, "bwd_mix"),
                    "step": {"gbs": round(step_b / (ms_step * 1e-3) / 1e9, 1),
                             "mtokens_per_s": round(S / (ms_step * 1e-3) / 1e6, 2),
                             "frac_of_measured": round(step_b / (ms_step * 1e-3) / 1e9 / peak, 4)}},
@@ -382,12 +553,17 @@ def finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws
                      "achieved": round(bwd_achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(bwd_achieved / peak, 4),
+                     "ceiling_gbs": ceil["bwd_mix"]["gbs"],
+                     "frac_of_ceiling": round(bwd_achieved / ceil["bwd_mix"]["gbs"], 4),
+                     "frac_of_8tbs_nominal": round(bwd_achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": tr, "algorithmic_bytes": bwd_b},
+        "ceiling": ceil,
         "e2e": None if e2e is None else {
             "value": round(ws * step_b / (e2e[0] * 1e-3) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(e2e[0], 3), "h2d_bytes_per_step": e2e[1],
             "d2h_bytes_per_step": e2e[2]},
         "gpu_launches": 3 * K,
+        **({"routes": extra["routes"]} if "routes" in extra else {}),
         "clocks": clocks,
         "kernel_sha": sha,
     }
@@ -420,6 +596,31 @@ def oracle_slice(w, tokens):
     return x, dy, w.weight.cpu(), None if w.bias is None else w.bias.cpu(), cu, n, np
 
 
+def oracle_channel_sharded(x, dy, W, b, cu, policy, nthreads):
+    """The oracle, as it is, on channel slices in nthreads host threads (its
+    C calls release the interpreter lock; channels are independent, so the
+    values are those of one call over all channels)."""
+    import concurrent.futures
+
+    import oracle
+
+    C = x.shape[1]
+    bounds = [C * i // nthreads for i in range(nthreads + 1)]
+
+    def job(i):
+        c0, c1 = bounds[i], bounds[i + 1]
+        if c1 <= c0:
+            return
+        xs, gs = x[:, c0:c1].contiguous(), dy[:, c0:c1].contiguous()
+        bs = None if b is None else b[c0:c1]
+        oracle.fwd(xs, W[c0:c1], cu, bs)
+        oracle.bwd(xs, gs, W[c0:c1], cu, bs, policy)
+
+    oracle.load()
+    with concurrent.futures.ThreadPoolExecutor(nthreads) as ex:
+        list(ex.map(job, range(nthreads)))
+
+
 def cpu_baseline(w, policy, tokens):
     import oracle
 
@@ -429,10 +630,19 @@ def cpu_baseline(w, policy, tokens):
     oracle.bwd(x, dy, W, cu, b, policy)
     dt = time.perf_counter() - t0
     fwd_b, bwd_b = compulsory_bytes(n, w.C, 0)
+    nproc = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle_channel_sharded(x, dy, W, b, cu, policy, nproc)
+    dt_all = time.perf_counter() - t0
     return {"value": round((fwd_b + bwd_b) / dt / 1e9, 5), "unit": "GB/s", "cores": 1,
             "kind": "oracle", "seconds": round(dt, 2),
+            "mtokens_per_s": round(n / dt / 1e6, 6), "host_nproc": nproc,
             "sample": f"first {n} tokens x all {w.C} channels of the same workload, "
-                      f"fwd + bwd ({policy}), single-threaded FP64 C"}
+                      f"fwd + bwd ({policy}), single-threaded FP64 C",
+            "all_cores": {"value": round((fwd_b + bwd_b) / dt_all / 1e9, 5), "unit": "GB/s",
+                          "cores": nproc, "seconds": round(dt_all, 2),
+                          "mtokens_per_s": round(n / dt_all / 1e6, 6),
+                          "sample": f"the same slice split by channels over {nproc} threads"}}
 
 
 def ref_tokens(args, C):
@@ -498,6 +708,8 @@ def main():
                          "when --steps is large, so the arm's K steps take about a minute)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the per-workload / per-policy timings (routes)")
     ap.add_argument("--S", type=int, default=None,
                     help="scale the workload to S tokens (same recipe); profiling runs only")
     ap.add_argument("--policy", choices=["bf16", "fp32"], default=None,

@@ -44,7 +44,8 @@ typedef enum { VCD_BF16 = 0, VCD_FP32 = 1 } vcd_dtype;
 
 /* Where SiLU' is evaluated in the backward ("silu_grad_preactivation" on the
  * backward page, Parameters): at the BF16-rounded recomputed preactivation,
- * or at the unrounded FP32 preactivation (with an FP64 final reduction). */
+ * or at the unrounded FP32 preactivation (with a final reduction as exact as
+ * an FP64 one, in compensated FP32 arithmetic). */
 typedef enum { VCD_SILU_GRAD_BF16 = 0, VCD_SILU_GRAD_FP32 = 1 } vcd_silu_policy;
 
 typedef enum {
@@ -63,17 +64,18 @@ int conv1d_fwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
 
 /* Bytes of backward workspace for (S, C): the FP32 partial rows of dweight
  * and dbias (backward page, Parameters: workspace). A function of (S, C)
- * alone: the maximum over every route (bias or not, dtypes, policy; the
- * "fp32" policy cuts shorter work units and needs the most) and the same on
- * every device, so one buffer serves every call of that shape. The kernel
+ * alone: the maximum over every route (bias or not, dtypes, policy, launch
+ * shape) and the same on every device, so one buffer serves every call of
+ * that shape: one row of 128 channels x 5 FP32 values (2560 bytes) per chunk
+ * of work of each 128-channel column, at most max(2432, ceil(C / 128)) rows. The kernel
  * writes every byte it later reads: the buffer needs no zeroing. Same errors
  * as the forward query. */
 int conv1d_bwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
 
 /* Bytes of backward workspace one policy needs (backward page, Parameters:
  * workspace): the partial rows of the
- * "bf16" (policy 0) or "fp32" (policy 1) program for (S, C), the larger of
- * its two launch shapes; at most conv1d_bwd_workspace_size(S, C). Every
+ * "bf16" (policy 0) or "fp32" (policy 1) program for (S, C), the largest
+ * over its launch shapes; at most conv1d_bwd_workspace_size(S, C). Every
  * conv1d_bwd call of that policy accepts a workspace of this size. Errors as
  * the queries above, plus VCD_ERR_INVALID_ARG for an unknown policy. */
 int conv1d_bwd_route_workspace_size(int64_t S, int64_t C, int policy, size_t* bytes);
@@ -81,10 +83,11 @@ int conv1d_bwd_route_workspace_size(int64_t S, int64_t C, int policy, size_t* by
 /* Bytes of backward workspace one call needs, exactly (backward page,
  * Parameters: workspace): the partial rows that
  * conv1d_bwd writes and reads for these arguments (has_bias: a bias is
- * passed). The call picks one of two launch shapes from them -- 16 warps per
- * SM for the "fp32" policy, for documents shorter than 32 tokens on average
- * (num_docs * 32 >= S) and for calls without a bias; 12 warps with more
- * registers otherwise -- and the shape sets the number of work units. At most
+ * passed). The call picks one of three launch shapes from them -- for the
+ * "bf16" policy 16 warps per SM when documents are shorter than 32 tokens on
+ * average (num_docs * 32 >= S) or there is no bias, 12 warps with more
+ * registers otherwise; for the "fp32" policy 12 warps with shared memory for
+ * its chunk sums -- and the shape sets the number of chunks. At most
  * conv1d_bwd_route_workspace_size(S, C, policy). Errors as
  * conv1d_bwd_route_workspace_size, plus VCD_ERR_INVALID_ARG for S > 0 with
  * num_docs <= 0. */
@@ -117,10 +120,15 @@ int conv1d_fwd(const void* x, int64_t S, int64_t C,
  *   dweight[c, k] = sum_t dpre[t, c] * x[t - 3 + k, c]             (zero history)
  *   dbias[c]      = sum_t dpre[t, c]                               (if dbias != NULL)
  * with dpre = dy * silu'(p). Two launches on `stream`: the main kernel writes
- * dx and one FP32 partial row per work unit into the workspace, and a reduce
- * kernel, launched programmatically dependent on it, sums the rows in a fixed
- * order (FP32 under VCD_SILU_GRAD_BF16, FP64 under VCD_SILU_GRAD_FP32), so the
- * gradients are bitwise identical for a given (S, C) and route.
+ * dx and one FP32 partial row per chunk of work into the workspace, and a
+ * reduce kernel, launched programmatically dependent on it, sums the rows in
+ * a fixed order, so the gradients are bitwise identical for a given (S, C)
+ * and route. Under VCD_SILU_GRAD_BF16 a chunk is one run of tokens summed in
+ * FP32 and the reduce adds in FP32. Under VCD_SILU_GRAD_FP32 a chunk is
+ * several runs of at most 256 tokens, each summed in FP32 and added into the
+ * chunk's total with compensated (two-float) additions; the reduce adds the
+ * chunk totals the same way, which keeps the sum as exact as an FP64
+ * accumulator would before its one rounding to the output dtype.
  *   x, dy     [S, C] BF16, read.
  *   weight, cu_seqlens, num_docs, bias   as in conv1d_fwd (bias must be the
  *             forward's bias: it enters the preactivation).
@@ -144,11 +152,10 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C,
                cudaStream_t stream);
 
 /* Size of the fixed device scratch used by conv1d_bwd_noalloc: 8 MiB. Under
- * the "bf16" policy that holds the partial rows of every shape with
- * C <= 419328 (at most 2432 rows of 2560 bytes, 6.2 MB, while C <= 311296;
- * one row per 128-channel column above that); the "fp32" policy uses one row
- * per 256 tokens of each 128-channel column (2560 bytes each), so it fits
- * while ceil(S / 256) * ceil(C / 128) <= 3276, e.g. S <= 17408 at C = 6144. */
+ * either policy that holds the partial rows of every shape with
+ * C <= 419328: at most max(2432, ceil(C / 128)) rows of 2560 bytes, i.e. at
+ * most 6.2 MB while C <= 311296, and one row per 128-channel column above
+ * that. */
 #define VCD_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* Backward without a workspace argument and without any allocation. The
@@ -158,7 +165,7 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C,
  * or code that must not call cudaMalloc/cudaFree once it is running (those
  * calls can stall every stream on the device). It computes exactly what
  * conv1d_bwd computes, with the same arguments minus workspace and
- * workspace_bytes, and keeps the per-unit partial rows in a fixed
+ * workspace_bytes, and keeps the partial rows in a fixed
  * VCD_NOALLOC_SCRATCH_BYTES array compiled into the library, which every GPU
  * that loads the library holds until the process exits.
  *   - Shapes whose partial rows exceed VCD_NOALLOC_SCRATCH_BYTES are refused
@@ -169,7 +176,9 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C,
  *     capturing uses the remembered address. Make one call on a device before
  *     capturing calls on it: a first call made during capture runs that lookup
  *     (and the kernels' one-time set-up: shared-memory attribute and occupancy
- *     queries) inside the capture.
+ *     queries) inside the capture. On GB300 with CUDA 13.0 such a first call
+ *     was seen to succeed, its graph replaying the eager call's bits, but
+ *     that order is not relied on.
  *   - Every call shares the one array. It needs no clearing (each call writes
  *     all the rows it reads), but two calls whose kernels may overlap on the
  *     GPU -- different streams, no ordering between them -- race on it and

@@ -13,12 +13,14 @@ from varlen_causal_depthwise_gb300 import binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "vcd.h")
+STREAM_HEADER = os.path.join(ROOT, "include", "vcd_stream.h")
 
 
-def declared():
-    text = open(HEADER).read()
+def declared(header=HEADER, prefix="conv1d_"):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(conv1d_\w+)\s*\(", text, re.M)))
+    pat = r"^\s*(?:const\s+)?\w+\*?\s+\*?(" + prefix + r"\w+)\s*\("
+    return sorted(set(re.findall(pat, text, re.M)))
 
 
 @pytest.fixture(scope="module")
@@ -38,6 +40,12 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_stream_header_declares_the_ceiling_kernel(lib):
+    assert declared(STREAM_HEADER, "vcd_") == sorted(binding.STREAM_SIGNATURES)
+    for name in declared(STREAM_HEADER, "vcd_"):
+        assert hasattr(lib, name), name
+
+
 def test_status_strings(lib):
     assert vcd.conv1d_status_string(0) == "ok"
     for s in range(1, 5):
@@ -50,17 +58,18 @@ def test_workspace_queries(lib):
     assert vcd.conv1d_bwd_workspace_size(0, 256) == 0
     n = vcd.conv1d_bwd_workspace_size(65536, 6144)
     assert n > 0 and n % 16 == 0
-    # one FP32 row of 128 channels x 5 values per work unit; the "fp32" policy
-    # (one unit per 256 tokens of each of the 48 columns) needs the most
-    assert n == 48 * (65536 // 256) * 128 * 5 * 4
     for bad in ((-1, 8), (8, 0), (8, 12)):
         with pytest.raises(vcd.VcdError):
             vcd.conv1d_bwd_workspace_size(*bad)
     bf, fp = (vcd.conv1d_bwd_route_workspace_size(65536, 6144, p) for p in ("bf16", "fp32"))
-    assert bf < fp == n
-    # one row per warp-sized unit; the larger of the policy's two launch shapes
-    # (16 warps per SM: 48 columns x 50 rows = 2400 units)
+    assert max(bf, fp) == n
+    # one FP32 row of 128 channels x 5 values per chunk of a column. "bf16":
+    # one warp-sized unit per chunk, the larger of the two launch shapes (16
+    # warps per SM: 48 columns x 50 rows = 2400 units)
     assert bf == 48 * 50 * 128 * 5 * 4
+    # "fp32": 256-token units (256 per column), 7 to a chunk so that the 38
+    # warps per column of the chunked shape each take about one: 37 chunks
+    assert fp == 48 * 37 * 128 * 5 * 4
     with pytest.raises(ValueError):
         vcd.conv1d_bwd_route_workspace_size(8, 8, "fp16")
 
@@ -76,7 +85,7 @@ def test_call_workspace_query_follows_the_launch_shape(lib):
     assert call(S, C, 20, "bf16", False) == 48 * 50 * row          # deep: 2400 units
     assert call(S, C, S // 32, "bf16", True) == 48 * 50 * row      # short documents: deep
     assert call(S, C, S // 32 - 1, "bf16", True) == 48 * 38 * row
-    assert call(S, C, 20, "fp32", True) == call(S, C, 20, "fp32", False) == 48 * 256 * row
+    assert call(S, C, 20, "fp32", True) == call(S, C, 20, "fp32", False) == 48 * 37 * row  # chunks
     for S_, C_, nd in ((4096, 256, 4), (131072, 1032, 52000), (300, 40, 3), (1, 8, 1)):
         for pol in ("bf16", "fp32"):
             for hb in (True, False):
@@ -172,9 +181,9 @@ def test_binding_rejects_host_tensors_before_any_call():
 def test_workspace_queries_are_consistent(lib):
     """Random shapes: the per-call need is a whole number of 2560-byte partial
     rows, never above its policy's need, which is never above the need of every
-    route; the policy's need is the larger of its launch shapes' needs (16 warps
-    for short documents or no bias, 12 warps with a bias), and the "fp32"
-    policy always takes the same shape."""
+    route; the "bf16" policy's need is the larger of its launch shapes' needs
+    (16 warps for short documents or no bias, 12 warps with a bias), and the
+    "fp32" policy always takes the same (chunked) shape."""
     rng = np.random.default_rng(2024)
     call = vcd.conv1d_bwd_call_workspace_size
     for _ in range(300):
@@ -205,11 +214,13 @@ def test_noalloc_scratch_size_matches_the_header():
 
 
 @pytest.mark.parametrize("S,C,policy,fits", [
-    (17408, 6144, "fp32", True),        # ceil(S/256) * 48 columns = 3264 rows <= 3276
-    (17664, 6144, "fp32", False),       # 69 * 48 = 3312 rows
     (1 << 20, 419328, "bf16", True),    # 3276 columns of one row each
     (1 << 20, 419336, "bf16", False),   # 3277 columns
+    (1 << 20, 419328, "fp32", True),
+    (1 << 20, 419336, "fp32", False),
     (262144, 311296, "bf16", True),
+    (262144, 8192, "fp32", True),       # 64 columns x 28 chunks
+    ((1 << 31) - 128, 6144, "fp32", True),
 ])
 def test_noalloc_limits_stated_in_the_header(lib, S, C, policy, fits):
     """The shapes include/vcd.h names on either side of the fixed scratch's

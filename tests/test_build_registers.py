@@ -2,13 +2,14 @@
 
 The backward picks its launch shape on the host from the route: the wide shape
 (12 warps, up to 168 registers) for "bf16"-policy calls with a bias and longer
-documents, the deep shape (16 warps, at most 128 registers) otherwise. That
-rule rests on the compiled kernels: every wide-shape kernel and every forward
-kernel (both batch shapes) keeps its state in registers, and so do the deep
-shape's "bf16"-policy kernels without a bias. A source change that makes one of
-those spill silently makes its route slower, so this test compiles the kernels
-with ptxas' resource report and checks the spill counts. CPU only (nvcc
-cross-compiles for sm_103a).
+documents, the deep shape (16 warps, at most 128 registers) for the other
+"bf16"-policy calls, and the chunked shape (12 warps, up to 168 registers) for
+the "fp32" policy. That rule rests on the compiled kernels: every wide-shape
+and chunked-shape kernel and every forward kernel (both batch shapes) keeps its
+state in registers, and so do the deep shape's kernels without a bias. A
+source change that makes one of those spill silently makes its route slower,
+so this test compiles the kernels with ptxas' resource report and checks the
+spill counts. CPU only (nvcc cross-compiles for sm_103a).
 """
 import concurrent.futures
 import os
@@ -80,17 +81,29 @@ def test_forward_kernels_do_not_spill(resources):
 def test_backward_shapes_fit_their_register_budgets(resources):
     _, bwd = resources
     k = _main_kernels(bwd)
-    # wide shape: "bf16" policy with a bias only, every weight dtype x bias dtype x chunk form
+    # wide: "bf16" policy with a bias, one unit per chunk; deep: "bf16" policy,
+    # every bias kind, one unit per chunk; chunked: "fp32" policy, both forms
     wide = {key: r for key, r in k.items() if key[0] == 0}
     deep = {key: r for key, r in k.items() if key[0] == 1}
-    assert len(wide) == 8 and len(deep) == 24
-    assert all(key[3] == 0 and key[2] != 0 for key in wide)
+    chunked = {key: r for key, r in k.items() if key[0] == 2}
+    assert len(wide) == 4 and len(deep) == 6 and len(chunked) == 12
+    assert all(key[3] == 0 and key[2] != 0 and key[4] == 0 for key in wide)
+    assert all(key[3] == 0 and key[4] == 0 for key in deep)
+    assert all(key[3] == 1 for key in chunked)
+    for key, (regs, st, ld) in list(wide.items()) + list(chunked.items()):
+        assert regs <= 168, f"{key}: {regs} registers"
     for key, (regs, st, ld) in wide.items():
-        assert regs <= 168 and st == 0 and ld == 0, f"wide {key}: {regs} registers, spills {st}/{ld}"
+        assert st == 0 and ld == 0, f"wide {key}: {regs} registers, spills {st}/{ld}"
+    for key, (regs, st, ld) in chunked.items():
+        # the multi-unit form every large "fp32" call takes: at most one spilled
+        # word (with the packed accurate SiLU' some routes spill 4 bytes, and
+        # still run faster than the scalar form without spills, measured)
+        if key[4] == 1:
+            assert st <= 4 and ld <= 4, f"chunked {key}: {regs} registers, spills {st}/{ld}"
     for key, (regs, st, ld) in deep.items():
         assert regs <= 128, f"deep {key}: {regs} registers"
     # the deep shape runs mask-free "bf16" calls only where it keeps everything
-    # in registers: the routes without a bias (single-unit chunks)
+    # in registers: the routes without a bias
     for wb in (0, 1):
         regs, st, ld = deep[(1, wb, 0, 0, 0)]
         assert st == 0 and ld == 0, f"deep bf16 no-bias (weight bf16={wb}) spills {st}/{ld} bytes"

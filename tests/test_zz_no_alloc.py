@@ -72,10 +72,10 @@ def test_noalloc_refuses_shapes_beyond_its_scratch():
         vcd.conv1d_bwd_noalloc(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, "bf16")
 
 
-def test_noalloc_fp32_policy_at_its_stated_limit():
-    """S = 17408 at C = 6144: the largest "fp32"-policy shape the header says
-    fits the fixed scratch (3264 of its 3276 rows)."""
-    S, C = 17408, 6144
+def test_noalloc_fp32_policy_on_a_chunked_shape():
+    """The "fp32" policy at S = 65536, C = 6144: 256-token units folded seven
+    to a chunk, 1776 chunk rows of the fixed scratch's 3276."""
+    S, C = 65536, 6144
     w = synth.make("linattn", device=DEV, S=S, C=C)
     ref = vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, "fp32",
                          dweight=torch.empty(C, 4, device=DEV), dbias=torch.empty(C, device=DEV))

@@ -40,6 +40,11 @@ SIGNATURES = {
     "conv1d_status_string": (ctypes.c_char_p, [_int]),
 }
 
+# include/vcd_stream.h: the bandwidth-ceiling kernel (no part of the operation).
+STREAM_SIGNATURES = {
+    "vcd_stream_copy": (_int, [_vp, _vp, _vp, _sz, _int, _vp]),
+}
+
 
 class VcdError(RuntimeError):
     def __init__(self, status, where):
@@ -61,7 +66,7 @@ def load_library():
                 f"{path} is missing: build it with `python -m varlen_causal_depthwise_gb300.build`"
                 " (or __graft_entry__.build()); there is no CPU fallback")
         lib = ctypes.CDLL(path)
-        for name, (res, args) in SIGNATURES.items():
+        for name, (res, args) in {**SIGNATURES, **STREAM_SIGNATURES}.items():
             fn = getattr(lib, name)
             fn.restype, fn.argtypes = res, args
         _lib = lib
@@ -260,3 +265,19 @@ def conv1d_bwd_noalloc(x, dy, weight, cu_seqlens, bias=None, policy="bf16", dx=N
                                     _dt(dweight), _ptr(dbias), _dt(dbias), _stream(stream, dev))
     _check(st, "conv1d_bwd_noalloc")
     return dx, dweight, dbias
+
+
+def stream_copy(a, out, b=None, blocks_per_sm=2, stream=None):
+    """out = a (or a XOR b) byte for byte through vcd_stream_copy: the traffic
+    of a forward (a -> out) or a backward (a, b -> out) call with no
+    arithmetic. Tensors: CUDA, contiguous, same byte size."""
+    n = a.numel() * a.element_size()
+    for t, name in ((a, "a"), (out, "out"), (b, "b")):
+        if t is None:
+            continue
+        _require(t, name, (t.dtype,), a.device)
+        if t.numel() * t.element_size() != n:
+            raise ValueError(f"{name} must hold {n} bytes")
+    st = load_library().vcd_stream_copy(_ptr(a), _ptr(b), _ptr(out), n, int(blocks_per_sm),
+                                        _stream(stream, a.device))
+    _check(st, "vcd_stream_copy")

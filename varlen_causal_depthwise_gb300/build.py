@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "libvcd.so")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["vcd_fwd.cu", "vcd_bwd.cu", "vcd_capi.cu", "vcd_noalloc.cu"]
+SOURCES = ["vcd_fwd.cu", "vcd_bwd.cu", "vcd_capi.cu", "vcd_noalloc.cu", "vcd_stream.cu"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -60,6 +60,7 @@ constexpr int kBwdRowBytes = 2 * kBwdColCh;               // bytes of a token's 
 template <int SHAPE> struct BwdGeom;
 template <> struct BwdGeom<kBwdWide> { static constexpr int kWarps = 12, kNs = 3, kU = 12; };
 template <> struct BwdGeom<kBwdDeep> { static constexpr int kWarps = 16, kNs = 2, kU = 8; };
+template <> struct BwdGeom<kBwdChunked> { static constexpr int kWarps = 12, kNs = 3, kU = 8; };
 template <int SHAPE> struct BwdShapeT : BwdGeom<SHAPE> {
     using G = BwdGeom<SHAPE>;
     static constexpr int kThreads = 32 * G::kWarps;
@@ -70,7 +71,29 @@ template <int SHAPE> struct BwdShapeT : BwdGeom<SHAPE> {
     static_assert(G::kU % 2 == 0 && G::kU <= 30 && G::kNs >= 2, "batch geometry");
     static_assert(kSmemBytes <= 227 * 1024, "ring exceeds the shared memory of one CTA");
     static_assert(kBwdShapeWarps[SHAPE] == G::kWarps, "plan and kernel disagree on the shape");
+    // Chunks of several units (SEG): each lane's compensated chunk sums, hi
+    // and lo of its 5 * kBwdVec values, after the rings ([warp][value][lane]).
+    static constexpr int kAccFloats = 2 * kPartialStride * kBwdVec;
+    static constexpr int kSegSmemBytes = kSmemBytes + G::kWarps * kAccFloats * 32 * 4;
 };
+// Units of several per chunk are the "fp32" policy's, kFp32TokensPerUnit
+// tokens long; a multiple of the batch puts every unit boundary at the same
+// position of a batch.
+static_assert(kFp32TokensPerUnit % BwdGeom<kBwdDeep>::kU == 0, "unit boundaries must align");
+static_assert(kFp32TokensPerUnit % BwdGeom<kBwdChunked>::kU == 0, "unit boundaries must align");
+static_assert(BwdShapeT<kBwdDeep>::kSegSmemBytes <= 227 * 1024, "accumulators do not fit");
+static_assert(BwdShapeT<kBwdChunked>::kSegSmemBytes <= 227 * 1024, "accumulators do not fit");
+
+// hi + lo += v with the rounding error of hi + v carried into lo (the
+// two-sum of Knuth): summing n values keeps hi + lo within about
+// n 2^-48 of the exact sum relative to the sum of magnitudes.
+__device__ __forceinline__ void acc_two_sum(float& hi, float& lo, float v) {
+    const float s = __fadd_rn(hi, v);
+    const float bv = __fsub_rn(s, hi);
+    const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bv)), __fsub_rn(v, bv));
+    hi = s;
+    lo = __fadd_rn(lo, e);
+}
 
 constexpr int kPolicyBF16 = 0;
 constexpr int kPolicyFP32 = 1;
@@ -83,9 +106,11 @@ __device__ __forceinline__ float2 grad_at(float2 pre) {
     return silu_grad2_accurate(pre);
 }
 
-// SEG: a warp's chunk holds several units (the "fp32" policy's short units);
-// without it every chunk is a single unit and the unit-boundary logic compiles
-// away.
+// SEG: a warp's chunk holds several units (the "fp32" policy's short units),
+// whose sums it adds into compensated accumulators in shared memory at each
+// unit boundary; the chunk writes one partial row. Without SEG every chunk is
+// a single unit, the unit-boundary logic compiles away, and the unit's
+// register sums are its row.
 template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG>
 __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel(const BwdArgs a) {
     using SH = BwdShapeT<SHAPE>;
@@ -99,7 +124,7 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
     const int64_t warp0 = (int64_t)blockIdx.x * SH::kWarps + wid;
     const int64_t nwarps = (int64_t)gridDim.x * SH::kWarps;
     const int64_t S = a.plan.S, C = a.plan.C, L = a.plan.L;
-    const int64_t units = a.plan.units, ncols = a.plan.ncols;
+    const int64_t ncols = a.plan.ncols;
     const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(a.x);
     const __nv_bfloat16* __restrict__ dy = static_cast<const __nv_bfloat16*>(a.dy);
     __nv_bfloat16* __restrict__ dx = static_cast<__nv_bfloat16*>(a.dx);
@@ -107,21 +132,21 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
     const int ncu = (int)(a.num_docs + 1);
     const int Ci = (int)C;                               // row stride, elements
 
-    // Assignment. Each column's rows are cut into chunks of `per` consecutive
-    // rows, about one chunk per resident warp, and a warp streams a whole
-    // chunk as one segment: a pipeline restart happens per chunk, not per
-    // unit. Chunks are dealt row-major (consecutive warps take consecutive
-    // columns of the same chunk), so warps running side by side read whole
-    // token rows. Unit (row, col) always owns partial row row * ncols + col,
-    // whichever warp computes it.
-    // Without SEG every chunk is one unit and the loop is over units.
+    // Assignment. Each column's units are cut into chunks of `per` consecutive
+    // units (the plan's, from constants), and a warp streams a whole chunk as
+    // one segment: a pipeline restart happens per chunk, not per unit. Chunks
+    // are dealt row-major (consecutive warps take consecutive columns of the
+    // same chunk), so warps running side by side read whole token rows. Chunk
+    // (chunk, col) owns partial row chunk * ncols + col, whichever warp
+    // computes it. Without SEG every chunk is one unit.
     const int64_t rows = a.plan.rows;
-    const int64_t warps_per_col = nwarps / ncols > 0 ? nwarps / ncols : 1;
-    const int64_t per = SEG ? (rows + warps_per_col - 1) / warps_per_col : 1;
-    const int64_t n_asg = SEG ? ncols * ((rows + per - 1) / per) : units;
+    const int64_t per = SEG ? a.plan.per : 1;
+    const int64_t n_asg = ncols * a.plan.chunks;
+    float* const acc = reinterpret_cast<float*>(smem + SH::kSmemBytes) +
+                       wid * SH::kAccFloats * 32 + lane;        // SEG: [value][lane] of this warp
     for (int64_t asg = warp0; asg < n_asg; asg += nwarps) {
         const int64_t col = asg % ncols, chunk = asg / ncols;
-        const int64_t row0 = SEG ? chunk * per : chunk;
+        const int64_t row0 = chunk * per;
         const int64_t row1 = !SEG ? row0 + 1 : row0 + per < rows ? row0 + per : rows;
         const int64_t c0 = col * kBwdColCh + lane * kBwdVec;
         const bool active = c0 < C;
@@ -136,7 +161,6 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
         const int r_du = (int)(u_end - q0);
         const int nb = (r_end + 3 + kBwdU - 1) / kBwdU;
         const int Li = (int)L;
-        int64_t cur_row = row0;                                   // unit being accumulated
         int r_next = SEG && row1 - row0 > 1 ? 3 + Li : INT_MAX;   // where the next unit starts
 
         // The first batches' copies go out before the taps and the document
@@ -177,34 +201,58 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
             db[p] = zero2();
         }
 
-        // Write the finished unit's partial row ([kBwdColCh channels][5] FP32;
-        // this lane's kBwdVec channels are 5 * kBwdVec consecutive floats) and
-        // start the next unit's sums from zero.
-        auto flush = [&](int64_t unit_row) {
-            if (active) {
-                float r[kBwdVec][kPartialStride];
-#pragma unroll
-                for (int p = 0; p < kNP; ++p) {
-#pragma unroll
-                    for (int k = 0; k < 5; ++k) {
-                        const float2 val = k < 4 ? dw[k][p] : db[p];
-                        r[2 * p][k] = val.x;
-                        r[2 * p + 1][k] = val.y;
-                    }
-                }
-                const int64_t unit = unit_row * ncols + col;
-                float2* dst = reinterpret_cast<float2*>(
-                    a.partials + (unit * kBwdColCh + lane * kBwdVec) * kPartialStride);
-                const float* flat = &r[0][0];
-#pragma unroll
-                for (int i = 0; i < kBwdVec * kPartialStride / 2; ++i)
-                    dst[i] = make_float2(flat[2 * i], flat[2 * i + 1]);
-            }
+        // This lane's sums in row order: channel c0 + i's five values at
+        // 5 i .. 5 i + 4 (dweight taps 0..3, dbias).
+        auto sum_at = [&](int f) -> float {
+            const int ch = f / kPartialStride, k = f % kPartialStride;
+            const float2 v = k < 4 ? dw[k][ch / 2] : db[ch / 2];
+            return (ch & 1) ? v.y : v.x;
+        };
+        auto clear_sums = [&]() {
 #pragma unroll
             for (int p = 0; p < kNP; ++p) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) dw[k][p] = zero2();
                 db[p] = zero2();
+            }
+        };
+        // SEG: the finished unit's sums into the chunk's accumulators.
+        auto fold_unit = [&]() {
+#pragma unroll
+            for (int f = 0; f < kPartialStride * kBwdVec; ++f)
+                acc_two_sum(acc[(2 * f) * 32], acc[(2 * f + 1) * 32], sum_at(f));
+            clear_sums();
+        };
+        if (SEG) {
+#pragma unroll
+            for (int f = 0; f < SH::kAccFloats; ++f) acc[f * 32] = 0.0f;
+        }
+        // Write the chunk's partial row ([kBwdColCh channels][5] FP32; this
+        // lane's kBwdVec channels are 5 * kBwdVec consecutive floats): the
+        // register sums of its one unit, or the rounded compensated sums.
+        auto write_row = [&]() {
+            if (SEG) fold_unit();
+            if (active) {
+                float2* dst = reinterpret_cast<float2*>(
+                    a.partials + ((chunk * ncols + col) * kBwdColCh + lane * kBwdVec) * kPartialStride);
+#pragma unroll
+                for (int i = 0; i < kBwdVec * kPartialStride / 2; ++i) {
+                    float v[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int f = 2 * i + h;
+                        v[h] = SEG ? __fadd_rn(acc[(2 * f) * 32], acc[(2 * f + 1) * 32]) : sum_at(f);
+                    }
+                    dst[i] = make_float2(v[0], v[1]);
+                }
+            }
+            if (!SEG) clear_sums();
+        };
+        // SEG: token r (at position 3 of its batch) starts the next unit.
+        auto unit_boundary = [&](int r) {
+            if (SEG && r == r_next) {
+                fold_unit();
+                r_next = r_next + Li < r_end ? r_next + Li : INT_MAX;
             }
         };
 
@@ -225,10 +273,13 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
             const unsigned char* sx = ring + slot * kBwdStageBytes + lane * (2 * kBwdVec);
             const unsigned char* sg = sx + kBwdTensorBytes;
 
-            if (M == 0 && r0 >= 6 && r0 + kBwdU <= r_end && (!SEG || r_next >= r0 + kBwdU)) {
-                // every token accumulates and emits dx three tokens back
+            // an interior batch: every token accumulates and emits dx three
+            // tokens back (a unit boundary, if any, is at position 3)
+            const bool interior = r0 >= 6 && r0 + kBwdU <= r_end;
+            if (M == 0 && interior) {
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
+                    if (j == 3) unit_boundary(r0 + j);
                     uint32_t xv[kNP], gv[kNP], o[kNP];
                     lds_pairs<kBwdVec>(sx + j * kBwdRowBytes, xv);
                     lds_pairs<kBwdVec>(sg + j * kBwdRowBytes, gv);
@@ -260,15 +311,58 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
                     }
                     if (active) st_pairs<kBwdVec>(dxq + j * Ci, o);
                 }
+            } else if (SHAPE != kBwdWide && interior) {
+                // Document starts inside: bit i of N1 / N2 / N3 is set when no
+                // document starts at bit i / at bits i, i+1 / at bits i..i+2
+                // of M, so each term's predicate is one bit of one mask. (The
+                // wide shape runs long documents only, and leaves its rare
+                // batches with a start to the general path below: a third
+                // copy of the loop makes its kernels spill.)
+                const uint32_t N1 = ~M, N2 = ~(M | (M >> 1)), N3 = ~(M | (M >> 1) | (M >> 2));
+#pragma unroll
+                for (int j = 0; j < kBwdU; ++j) {
+                    if (j == 3) unit_boundary(r0 + j);
+                    uint32_t xv[kNP], gv[kNP], o[kNP];
+                    lds_pairs<kBwdVec>(sx + j * kBwdRowBytes, xv);
+                    lds_pairs<kBwdVec>(sg + j * kBwdRowBytes, gv);
+                    // tap k of token t sees x[t-3+k] iff no start in (t-3+k, t];
+                    // dx[t-3] sees dpre[t-3+i] iff no start in (t-3, t-3+i]
+                    const bool m1 = bit(N1, j + 2), m2 = bit(N2, j + 1), m3 = bit(N3, j);
+                    const bool k1 = bit(N1, j), k2 = bit(N2, j);
+#pragma unroll
+                    for (int p = 0; p < kNP; ++p) {
+                        const float2 xf = bf16x2_to_float2(xv[p]);
+                        const float2 gf = bf16x2_to_float2(gv[p]);
+                        float2 pre = b[p];
+                        if (m3) pre = fma2<kPK>(w[0][p], xc[0][p], pre);
+                        if (m2) pre = fma2<kPK>(w[1][p], xc[1][p], pre);
+                        if (m1) pre = fma2<kPK>(w[2][p], xc[2][p], pre);
+                        pre = fma2<kPK>(w[3][p], xf, pre);
+                        const float2 d = mul2<kPK>(gf, grad_at<POLICY>(pre));
+                        if (m3) dw[0][p] = fma2<kPA>(d, xc[0][p], dw[0][p]);
+                        if (m2) dw[1][p] = fma2<kPA>(d, xc[1][p], dw[1][p]);
+                        if (m1) dw[2][p] = fma2<kPA>(d, xc[2][p], dw[2][p]);
+                        dw[3][p] = fma2<kPA>(d, xf, dw[3][p]);
+                        if (BIAS != kBiasNone) db[p] = add2<kPA>(db[p], d);
+                        float2 g = mul2<kPA>(w[3][p], dc[0][p]);
+                        if (k1) g = fma2<kPA>(w[2][p], dc[1][p], g);
+                        if (k2) g = fma2<kPA>(w[1][p], dc[2][p], g);
+                        if (m3) g = fma2<kPA>(w[0][p], d, g);
+                        o[p] = float2_to_bf16x2(g);
+                        xc[0][p] = xc[1][p];
+                        xc[1][p] = xc[2][p];
+                        xc[2][p] = xf;
+                        dc[0][p] = dc[1][p];
+                        dc[1][p] = dc[2][p];
+                        dc[2][p] = d;
+                    }
+                    if (active) st_pairs<kBwdVec>(dxq + j * Ci, o);
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
                     const int r = r0 + j;
-                    if (SEG && r == r_next) {             // token r starts the next unit
-                        flush(cur_row);
-                        ++cur_row;
-                        r_next = cur_row + 1 < row1 ? r_next + Li : INT_MAX;
-                    }
+                    if (j == 3) unit_boundary(r);
                     uint32_t xv[kNP], gv[kNP], o[kNP];
                     lds_pairs<kBwdVec>(sx + j * kBwdRowBytes, xv);
                     lds_pairs<kBwdVec>(sg + j * kBwdRowBytes, gv);
@@ -319,7 +413,7 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
             slot = slot + 1 == kBwdNs ? 0 : slot + 1;
         }
 
-        flush(cur_row);
+        write_row();
     }
     // Let the reduce kernel's CTAs be scheduled; its griddepcontrol.wait still
     // waits for this whole grid to finish and its writes to be visible.
@@ -328,26 +422,30 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
 
 // ------------------------------------------------------------- reduce ---
 
-template <typename T> __device__ __forceinline__ void store_out(void* base, int64_t i, T v, bool bf16);
-
-template <> __device__ __forceinline__ void store_out<float>(void* base, int64_t i, float v, bool bf16) {
-    if (bf16) reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
-    else reinterpret_cast<float*>(base)[i] = v;
+// The value hi + lo (|lo| at most half an ulp of hi, hi = fl(hi + lo)) in
+// BF16, rounded to nearest-even as the exact sum would be: hi's own rounding
+// unless hi lies exactly halfway between two BF16 values and lo decides the
+// side.
+__device__ __forceinline__ __nv_bfloat16 pair_to_bf16(float hi, float lo) {
+    const uint32_t u = __float_as_uint(hi);
+    if ((u & 0xffffu) != 0x8000u || lo == 0.0f) return __float2bfloat16_rn(hi);
+    const bool away = (lo > 0.0f) == (hi > 0.0f);            // the sum's magnitude exceeds |hi|
+    const uint32_t r = away ? (u & 0xffff0000u) + 0x10000u : (u & 0xffff0000u);
+    return __ushort_as_bfloat16((unsigned short)(r >> 16));
 }
-template <> __device__ __forceinline__ void store_out<double>(void* base, int64_t i, double v, bool bf16) {
-    if (bf16) reinterpret_cast<__nv_bfloat16*>(base)[i] = __double2bfloat16(v);
-    else reinterpret_cast<float*>(base)[i] = (float)v;
-}
 
-// Reduce: output (channel c, value k) is the sum over the R unit rows of its
+// Reduce: output (channel c, value k) is the sum over the R chunk rows of its
 // column. A CTA handles 32 outputs with n threads each (n = red_slices(R)):
 // thread s sums the fixed row slice [s R / n, (s + 1) R / n) in row order,
 // then thread 0 of the output adds the n slice sums in slice order. The order
 // depends on R only, so the result is bitwise reproducible per (S, C, route).
 // n grows with R (at least 8 rows a slice, at most 16 slices) so that each
-// thread's chain of dependent loads stays short: the "bf16" policy has a few
-// dozen rows per column (8 slices), the "fp32" policy one per 256 tokens
-// (1024 at S = 262144: 16 slices of 64 rows).
+// thread's chain of dependent loads stays short.
+// COMP (the "fp32" policy): every addition is compensated (two-sum into a
+// hi / lo pair), so the total is the rows' exact sum to about R 2^-48
+// relative to the sum of their magnitudes before its one final rounding --
+// what an FP64 accumulator would give, at FP32 rates (FP64 arithmetic runs at
+// a small fraction of FP32's on GB300).
 constexpr int kRedOutputs = 32;
 constexpr int kRedMaxSlices = 16;
 
@@ -357,11 +455,12 @@ inline int red_slices(int64_t rows) {
     return n;
 }
 
-template <typename ACC>
+template <bool COMP>
 __global__ void __launch_bounds__(kRedOutputs * kRedMaxSlices, 4) bwd_reduce_kernel(const BwdArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    __shared__ ACC part[kRedMaxSlices][kRedOutputs];
-    const Plan& P = a.plan;
+    __shared__ float part_hi[kRedMaxSlices][kRedOutputs];
+    __shared__ float part_lo[kRedMaxSlices][kRedOutputs];
+    const BwdPlan& P = a.plan;
     const int nsl = blockDim.x / kRedOutputs;
     const int o = threadIdx.x % kRedOutputs;          // consecutive threads: consecutive outputs
     const int sl = threadIdx.x / kRedOutputs;
@@ -372,9 +471,11 @@ __global__ void __launch_bounds__(kRedOutputs * kRedMaxSlices, 4) bwd_reduce_ker
     const int64_t col = c / kBwdColCh, ci = c % kBwdColCh;
     const float* src = a.partials + (col * kBwdColCh + ci) * kPartialStride + k;
     const int64_t stride = P.ncols * kBwdColCh * kPartialStride;
-    const int64_t r0 = P.rows * sl / nsl, r1 = P.rows * (sl + 1) / nsl;
-    ACC acc = 0;
-    if (valid && !(k == 4 && a.dbias == nullptr)) {
+    const int64_t R = P.chunks;
+    const int64_t r0 = R * sl / nsl, r1 = R * (sl + 1) / nsl;
+    float hi = 0.0f, lo = 0.0f;
+    const bool wanted = valid && !(k == 4 && a.dbias == nullptr);
+    if (wanted) {
         // batches of 8 independent loads; rows past r1 read nothing and add
         // zero, which leaves every sum and its order unchanged
         const int n = (int)(r1 - r0);
@@ -387,16 +488,40 @@ __global__ void __launch_bounds__(kRedOutputs * kRedMaxSlices, 4) bwd_reduce_ker
                 q += stride;
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc += (ACC)v[j];
+            for (int j = 0; j < 8; ++j) {
+                if (COMP) acc_two_sum(hi, lo, v[j]);
+                else hi += v[j];
+            }
         }
     }
-    part[sl][o] = acc;
+    part_hi[sl][o] = hi;
+    part_lo[sl][o] = lo;
     __syncthreads();
-    if (sl != 0 || !valid || (k == 4 && a.dbias == nullptr)) return;
-    ACC total = part[0][o];
-    for (int j = 1; j < nsl; ++j) total += part[j][o];
-    if (k < 4) store_out<ACC>(a.dweight, c * 4 + k, total, a.dweight_bf16 != 0);
-    else store_out<ACC>(a.dbias, c, total, a.dbias_bf16 != 0);
+    if (sl != 0 || !wanted) return;
+    hi = part_hi[0][o];
+    lo = part_lo[0][o];
+    for (int j = 1; j < nsl; ++j) {
+        if (COMP) {
+            acc_two_sum(hi, lo, part_hi[j][o]);
+            lo = __fadd_rn(lo, part_lo[j][o]);
+        } else {
+            hi += part_hi[j][o];
+        }
+    }
+    void* base = k < 4 ? a.dweight : a.dbias;
+    const int64_t at = k < 4 ? c * 4 + k : c;
+    const bool bf16 = (k < 4 ? a.dweight_bf16 : a.dbias_bf16) != 0;
+    if (COMP) {
+        // normalise: s = fl(hi + lo) and the exact remainder e
+        const float s = __fadd_rn(hi, lo);
+        const float bv = __fsub_rn(s, hi);
+        const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bv)), __fsub_rn(lo, bv));
+        if (bf16) reinterpret_cast<__nv_bfloat16*>(base)[at] = pair_to_bf16(s, e);
+        else reinterpret_cast<float*>(base)[at] = s;
+    } else {
+        if (bf16) reinterpret_cast<__nv_bfloat16*>(base)[at] = __float2bfloat16_rn(hi);
+        else reinterpret_cast<float*>(base)[at] = hi;
+    }
 }
 
 // -------------------------------------------------------------- launch ---
@@ -407,46 +532,52 @@ int prepare_main_t() {
     // read the occupancy; both are host-side queries. The cache entries are
     // atomic (host threads may get here at once; each stores the same value).
     using SH = BwdShapeT<SHAPE>;
+    constexpr int kSmem = SEG ? SH::kSegSmemBytes : SH::kSmemBytes;
     static std::atomic<int> occ[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     const int known = occ[dev].load(std::memory_order_relaxed);
     if (known > 0) return known;
     if (cudaFuncSetAttribute(bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, SH::kSmemBytes) != cudaSuccess)
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
         return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>,
-                                                      SH::kThreads, SH::kSmemBytes) != cudaSuccess)
+                                                      SH::kThreads, kSmem) != cudaSuccess)
         return 0;
     occ[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
-template <int SHAPE, bool W_BF16, int BIAS, int POLICY>
-cudaError_t launch_main_t(const BwdArgs& a, int sm_count, cudaStream_t stream) {
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG>
+cudaError_t launch_main_form(const BwdArgs& a, int sm_count, cudaStream_t stream) {
     using SH = BwdShapeT<SHAPE>;
-    // Occupancy is the same for both forms (same launch bounds and shared memory).
-    const int occ = prepare_main_t<SHAPE, W_BF16, BIAS, POLICY, false>();
-    if (occ <= 0 || prepare_main_t<SHAPE, W_BF16, BIAS, POLICY, true>() <= 0)
-        return cudaErrorInvalidConfiguration;
-    const int64_t ctas_needed = (a.plan.units + SH::kWarps - 1) / SH::kWarps;
+    const int occ = prepare_main_t<SHAPE, W_BF16, BIAS, POLICY, SEG>();
+    if (occ <= 0) return cudaErrorInvalidConfiguration;
+    const int64_t n_asg = a.plan.ncols * a.plan.chunks;
+    const int64_t ctas_needed = (n_asg + SH::kWarps - 1) / SH::kWarps;
     const int64_t resident = (int64_t)sm_count * occ;
     const int64_t grid = ctas_needed < resident ? ctas_needed : resident;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
     cfg.blockDim = dim3(SH::kThreads);
-    cfg.dynamicSmemBytes = SH::kSmemBytes;
+    cfg.dynamicSmemBytes = SEG ? SH::kSegSmemBytes : SH::kSmemBytes;
     cfg.stream = stream;
-    // the kernel cuts each column into chunks of `per` rows, one per warp
-    const int64_t nwarps = (int64_t)cfg.gridDim.x * SH::kWarps;
-    const int64_t wpc = nwarps / a.plan.ncols > 0 ? nwarps / a.plan.ncols : 1;
-    const int64_t per = (a.plan.rows + wpc - 1) / wpc;
-    if (per > 1) return cudaLaunchKernelEx(&cfg, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, true>, a);
-    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, false>, a);
+    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>, a);
 }
 
-template <typename ACC>
+// Chunks of several units come only from the "fp32" policy, which runs the
+// deep shape; every other route has one unit per chunk.
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY>
+cudaError_t launch_main_t(const BwdArgs& a, int sm_count, cudaStream_t stream) {
+    if constexpr (SHAPE != kBwdWide && POLICY == kPolicyFP32) {
+        if (a.plan.per > 1) return launch_main_form<SHAPE, W_BF16, BIAS, POLICY, true>(a, sm_count, stream);
+    }
+    if (a.plan.per > 1) return cudaErrorInvalidValue;
+    return launch_main_form<SHAPE, W_BF16, BIAS, POLICY, false>(a, sm_count, stream);
+}
+
+template <bool COMP>
 cudaError_t launch_reduce_t(const BwdArgs& a, cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -454,11 +585,11 @@ cudaError_t launch_reduce_t(const BwdArgs& a, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     const int64_t n = a.plan.C * kPartialStride;
     cfg.gridDim = dim3((unsigned)((n + kRedOutputs - 1) / kRedOutputs));
-    cfg.blockDim = dim3(kRedOutputs * red_slices(a.plan.rows));
+    cfg.blockDim = dim3(kRedOutputs * red_slices(a.plan.chunks));
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bwd_reduce_kernel<ACC>, a);
+    return cudaLaunchKernelEx(&cfg, bwd_reduce_kernel<COMP>, a);
 }
 
 }  // namespace
@@ -473,16 +604,17 @@ cudaError_t launch_bwd(const BwdArgs& a, int sm_count, cudaStream_t stream) {
         {nullptr, launch_main_t<kBwdWide, false, kBiasF32, kPolicyBF16>, launch_main_t<kBwdWide, false, kBiasBF16, kPolicyBF16>},
         {nullptr, launch_main_t<kBwdWide, true, kBiasF32, kPolicyBF16>, launch_main_t<kBwdWide, true, kBiasBF16, kPolicyBF16>}};
     static const L deep_bf16[2][3] = {VCD_ROW(kBwdDeep, false, kPolicyBF16), VCD_ROW(kBwdDeep, true, kPolicyBF16)};
-    static const L deep_fp32[2][3] = {VCD_ROW(kBwdDeep, false, kPolicyFP32), VCD_ROW(kBwdDeep, true, kPolicyFP32)};
+    static const L fp32_t[2][3] = {VCD_ROW(VCD_FP32_SHAPE, false, kPolicyFP32),
+                                   VCD_ROW(VCD_FP32_SHAPE, true, kPolicyFP32)};
 #undef VCD_ROW
     const int wi = a.weight_bf16 ? 1 : 0;
     const bool fp32 = a.policy == kPolicyFP32;
-    const L fn = fp32 ? (a.shape == kBwdDeep ? deep_fp32[wi][a.bias_kind] : nullptr)
+    const L fn = fp32 ? (a.shape == VCD_FP32_SHAPE ? fp32_t[wi][a.bias_kind] : nullptr)
                       : a.shape == kBwdWide ? wide_bf16[wi][a.bias_kind] : deep_bf16[wi][a.bias_kind];
     if (fn == nullptr) return cudaErrorInvalidValue;     // a shape bwd_shape never picks
     cudaError_t e = fn(a, sm_count, stream);
     if (e != cudaSuccess) return e;
-    return fp32 ? launch_reduce_t<double>(a, stream) : launch_reduce_t<float>(a, stream);
+    return fp32 ? launch_reduce_t<true>(a, stream) : launch_reduce_t<false>(a, stream);
 }
 
 }  // namespace vcd

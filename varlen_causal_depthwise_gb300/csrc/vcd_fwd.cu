@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
             const unsigned char* st = ring + slot * kFwdStageBytes + lane * (2 * kFwdVec);
             __nv_bfloat16* yq = yp + (int64_t)r0 * ystep;
 
-            if (M == 0 && r0 >= 3 && r0 + kFwdU <= n_rel) {
+            if (M == 0 && r0 >= 3 && r0 + kFwdU <= n_rel) {      // every token stored
 #pragma unroll
                 for (int j = 0; j < kFwdU; ++j) {
                     const uint2 xv = lds64(st + j * kFwdRowBytes);
@@ -175,6 +175,34 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
                         float2 pre = fma2<kPK>(w[0][p], xc[0][p], b[p]);
                         pre = fma2<kPK>(w[1][p], xc[1][p], pre);
                         pre = fma2<kPK>(w[2][p], xc[2][p], pre);
+                        pre = fma2<kPK>(w[3][p], xf[p], pre);
+                        o[p] = float2_to_bf16x2(silu2<kPKS>(pre));
+                        xc[0][p] = xc[1][p];
+                        xc[1][p] = xc[2][p];
+                        xc[2][p] = xf[p];
+                    }
+                    if (active) st_stream(yq + j * Ci, make_uint2(o[0], o[1]));
+                }
+            } else if (SHAPE == kFwdShortDocs && r0 >= 3 && r0 + kFwdU <= n_rel) {
+                // Short documents put a start in most batches. bit i of N1 /
+                // N2 / N3: no document start at bit i / at bits i, i+1 / at
+                // bits i..i+2 of M. (The streaming shape leaves the rare
+                // batches with a start to the general path below: a third
+                // copy of the loop slows its mask-free path, measured.)
+                const uint32_t N1 = ~M, N2 = ~(M | (M >> 1)), N3 = ~(M | (M >> 1) | (M >> 2));
+#pragma unroll
+                for (int j = 0; j < kFwdU; ++j) {
+                    const uint2 xv = lds64(st + j * kFwdRowBytes);
+                    const float2 xf[2] = {bf16x2_to_float2(xv.x), bf16x2_to_float2(xv.y)};
+                    // tap k of token t sees x[t-3+k] iff no document starts in (t-3+k, t]
+                    const bool m1 = bit(N1, j + 2), m2 = bit(N2, j + 1), m3 = bit(N3, j);
+                    uint32_t o[2];
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        float2 pre = b[p];
+                        if (m3) pre = fma2<kPK>(w[0][p], xc[0][p], pre);
+                        if (m2) pre = fma2<kPK>(w[1][p], xc[1][p], pre);
+                        if (m1) pre = fma2<kPK>(w[2][p], xc[2][p], pre);
                         pre = fma2<kPK>(w[3][p], xf[p], pre);
                         o[p] = float2_to_bf16x2(silu2<kPKS>(pre));
                         xc[0][p] = xc[1][p];

@@ -41,7 +41,7 @@ struct BwdArgs {
     int dweight_bf16;
     int dbias_bf16;
     int shape;                // BwdShape
-    Plan plan;                // bwd_plan(S, C, policy, shape)
+    BwdPlan plan;             // bwd_plan(S, C, policy, shape)
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, int sm_count, cudaStream_t stream);

@@ -52,8 +52,11 @@ enum FwdShape { kFwdStream = 0, kFwdShortDocs = 1 };
 //             latency of instruction-heavy paths (document masks in most
 //             batches, the "fp32" policy's SiLU').
 // bwd_shape() picks one per call.
-enum BwdShape { kBwdWide = 0, kBwdDeep = 1 };
-constexpr int kBwdShapeWarps[2] = {12, 16};
+//   kBwdChunked: 12 warps, up to 168 registers, 8-token batches and room in
+//             shared memory for compensated per-chunk sums -- the "fp32"
+//             policy's chunks of 256-token units.
+enum BwdShape { kBwdWide = 0, kBwdDeep = 1, kBwdChunked = 2 };
+constexpr int kBwdShapeWarps[3] = {12, 16, 12};
 
 // Mean document length (tokens) below which most batches hold a document
 // start and take the masked path.
@@ -71,9 +74,15 @@ inline int fwd_shape(int64_t S, int64_t num_docs) {
 // and wide with a bias, whose 16-warp kernels would spill registers. A
 // function of the call's arguments only, so a route's partial rows are the
 // same on every call and every device.
+#ifndef VCD_SHORT_DOCS_WIDE
+#define VCD_SHORT_DOCS_WIDE 0
+#endif
+#ifndef VCD_FP32_SHAPE
+#define VCD_FP32_SHAPE 2
+#endif
 inline int bwd_shape(int64_t S, int64_t num_docs, int policy, bool has_bias) {
-    if (policy == 1) return kBwdDeep;
-    if (num_docs * kShortDocTokens >= S) return kBwdDeep;
+    if (policy == 1) return VCD_FP32_SHAPE;
+    if (!VCD_SHORT_DOCS_WIDE && num_docs * kShortDocTokens >= S) return kBwdDeep;
     return has_bias ? kBwdWide : kBwdDeep;
 }
 
@@ -85,6 +94,15 @@ struct Plan {
     int64_t rows;     // token ranges per column
     int64_t L;        // tokens per range (the last range may be shorter)
     int64_t units;    // ncols * rows
+};
+
+// The backward's plan adds its chunks: consecutive units of one column that
+// one warp streams without restarting, each chunk one partial row. (Kept out
+// of Plan: the forward's kernel arguments stay as small as they were, which
+// its schedule was measured to depend on.)
+struct BwdPlan : Plan {
+    int64_t per;      // units per chunk
+    int64_t chunks;   // chunks per column
 };
 
 inline Plan make_plan(int64_t S, int64_t C, int vec, int64_t target_units) {
@@ -108,36 +126,48 @@ inline Plan fwd_plan(int64_t S, int64_t C) { return make_plan(S, C, kFwdVec, kFw
 
 // The "fp32" SiLU' policy keeps each unit's FP32 dweight / dbias sums short
 // (at most kFp32TokensPerUnit tokens, relative rounding error about
-// 0.2 * 2^-24 * sqrt(256) = 2e-7) and leaves the rest of the sum to the FP64
-// reduction over units; the "bf16" policy's 5e-5 tolerance allows long units.
+// 0.2 * 2^-24 * sqrt(256) = 2e-7); a warp streams a chunk of consecutive
+// units of one column and adds each unit's sums into a compensated two-float
+// accumulator, so the chunk's one partial row is its sum rounded once to
+// FP32. The "bf16" policy's 5e-5 tolerance allows long units (one per chunk).
+// Chunks are cut from GB300's resident warps per column (constants, not the
+// device at hand), so the partial rows and their reduction order are the same
+// on every device.
 #ifndef VCD_FP32_UNIT_TOKENS
 #define VCD_FP32_UNIT_TOKENS 256
 #endif
 constexpr int64_t kFp32TokensPerUnit = VCD_FP32_UNIT_TOKENS;
 
-inline Plan bwd_plan(int64_t S, int64_t C, int policy, int shape) {
-    Plan p = make_plan(S, C, kBwdVec, kGb300Sms * kBwdShapeWarps[shape]);
+inline BwdPlan bwd_plan(int64_t S, int64_t C, int policy, int shape) {
+    const int64_t warps = kGb300Sms * kBwdShapeWarps[shape];
+    BwdPlan p;
+    static_cast<Plan&>(p) = make_plan(S, C, kBwdVec, warps);
+    p.per = 1;
+    p.chunks = p.rows;
     if (policy == 1 && p.L > kFp32TokensPerUnit && S > 0) {
         p.L = kFp32TokensPerUnit;
         p.rows = (S + p.L - 1) / p.L;
         p.units = p.ncols * p.rows;
+        const int64_t wpc = warps / p.ncols > 0 ? warps / p.ncols : 1;   // warps per column
+        p.per = (p.rows + wpc - 1) / wpc;
+        p.chunks = (p.rows + p.per - 1) / p.per;
     }
     return p;
 }
 
 // Bytes of one route's partial rows: one FP32 row of 32 * kBwdVec channels x
-// 5 values per unit.
+// 5 values per chunk of each column.
 inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy, int shape) {
     if (S <= 0) return 0;
-    const Plan p = bwd_plan(S, C, policy, shape);
-    return (uint64_t)p.units * p.col_channels * kPartialStride * sizeof(float);
+    const BwdPlan p = bwd_plan(S, C, policy, shape);
+    return (uint64_t)p.chunks * p.ncols * p.col_channels * kPartialStride * sizeof(float);
 }
 
 // The most a policy's routes need over every call shape: the "fp32" policy
-// always runs the deep shape, the "bf16" policy either shape.
+// always runs the chunked shape, the "bf16" policy the wide or the deep one.
 inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy) {
+    if (policy == 1) return bwd_workspace_bytes_for(S, C, policy, VCD_FP32_SHAPE);
     const uint64_t d = bwd_workspace_bytes_for(S, C, policy, kBwdDeep);
-    if (policy == 1) return d;
     const uint64_t w = bwd_workspace_bytes_for(S, C, policy, kBwdWide);
     return w > d ? w : d;
 }
