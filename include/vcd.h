@@ -195,6 +195,17 @@ int conv1d_bwd_noalloc(const void* x, const void* dy, int64_t S, int64_t C,
                        void* dbias, int dbias_dtype,
                        cudaStream_t stream);
 
+/* The backward's main kernel stages x and dy through shared memory with
+ * tensor-map copies (TMA) whose arrival it awaits on barriers; each wait gives
+ * up after about a second of SM clocks (a copy takes microseconds), sets a
+ * device-side flag and leaves that call's outputs incomplete. This reads the
+ * flag into *flag (1 if any kernel gave up since the last read, else 0) and
+ * clears it. Unlike every other entry point it reads device memory and waits
+ * for the device (cudaMemcpyFromSymbol). No counterpart on the pages: a
+ * diagnostic of this implementation. Returns VCD_OK, VCD_ERR_INVALID_ARG for
+ * flag == NULL, or VCD_ERR_CUDA. */
+int conv1d_wait_fault(int* flag);
+
 /* Static description of a vcd_status code (never NULL). */
 const char* conv1d_status_string(int status);
 

@@ -467,3 +467,9 @@ def test_report_accuracy(capsys):
         for k, v in sorted(REL_REPORT.items()):
             if " full " in k:
                 print(f"  rel-L2 {k}: {v:.3g}")
+
+
+def test_no_tile_wait_gave_up():
+    """No backward kernel in this module's calls gave up waiting on a staged
+    tile (the device-side flag a bounded wait sets instead of hanging)."""
+    assert vcd.conv1d_wait_fault() is False

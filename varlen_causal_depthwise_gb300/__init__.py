@@ -10,7 +10,7 @@ from .binding import (  # noqa: F401
     VcdError, conv1d_bwd, conv1d_bwd_call_workspace_size, conv1d_bwd_noalloc,
     conv1d_bwd_route_workspace_size,
     conv1d_bwd_workspace_size, conv1d_fwd, conv1d_fwd_workspace_size,
-    conv1d_status_string, library_path, load_library,
+    conv1d_status_string, conv1d_wait_fault, library_path, load_library,
 )
 from .functional import (  # noqa: F401,E402
     CakeCausalConv1dFunction, cake_causal_conv1d_train_backward,

@@ -37,6 +37,7 @@ SIGNATURES = {
                           _vp, _int, _vp, _int, _vp, _sz, _vp]),
     "conv1d_bwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _int,
                                   _vp, _vp, _int, _vp, _int, _vp]),
+    "conv1d_wait_fault": (_int, [ctypes.POINTER(_int)]),
     "conv1d_status_string": (ctypes.c_char_p, [_int]),
 }
 
@@ -281,3 +282,11 @@ def stream_copy(a, out, b=None, blocks_per_sm=2, stream=None):
     st = load_library().vcd_stream_copy(_ptr(a), _ptr(b), _ptr(out), n, int(blocks_per_sm),
                                         _stream(stream, a.device))
     _check(st, "vcd_stream_copy")
+
+
+def conv1d_wait_fault():
+    """True if a backward kernel gave up waiting on a staged tile since the
+    last call (never in normal operation); clears the flag. Synchronous."""
+    flag = _int(0)
+    _check(load_library().conv1d_wait_fault(ctypes.byref(flag)), "conv1d_wait_fault")
+    return bool(flag.value)

@@ -46,6 +46,10 @@ namespace {
 #ifndef VCD_BWD_PACKED
 #define VCD_BWD_PACKED 0
 #endif
+// x and dy stages by tensor-map copies (1) or by per-lane cp.async (0).
+#ifndef VCD_BWD_TMA
+#define VCD_BWD_TMA 1
+#endif
 #ifndef VCD_BWD_PACKED_ACC
 #define VCD_BWD_PACKED_ACC 0
 #endif
@@ -74,15 +78,21 @@ template <int SHAPE> struct BwdShapeT : BwdGeom<SHAPE> {
     // Chunks of several units (SEG): each lane's compensated chunk sums, hi
     // and lo of its 5 * kBwdVec values, after the rings ([warp][value][lane]).
     static constexpr int kAccFloats = 2 * kPartialStride * kBwdVec;
-    static constexpr int kSegSmemBytes = kSmemBytes + G::kWarps * kAccFloats * 32 * 4;
+    static constexpr int kAccBytes = G::kWarps * kAccFloats * 32 * 4;
+    // the TMA ring's barriers: one 8-byte mbarrier per stage of each warp
+    static constexpr int kBarBytes = G::kWarps * G::kNs * 8;
+    template <bool SEG> static constexpr int smem_bytes() {
+        return kSmemBytes + (SEG ? kAccBytes : 0) + (VCD_BWD_TMA ? kBarBytes : 0);
+    }
 };
 // Units of several per chunk are the "fp32" policy's, kFp32TokensPerUnit
 // tokens long; a multiple of the batch puts every unit boundary at the same
 // position of a batch.
 static_assert(kFp32TokensPerUnit % BwdGeom<kBwdDeep>::kU == 0, "unit boundaries must align");
 static_assert(kFp32TokensPerUnit % BwdGeom<kBwdChunked>::kU == 0, "unit boundaries must align");
-static_assert(BwdShapeT<kBwdDeep>::kSegSmemBytes <= 227 * 1024, "accumulators do not fit");
-static_assert(BwdShapeT<kBwdChunked>::kSegSmemBytes <= 227 * 1024, "accumulators do not fit");
+static_assert(BwdShapeT<kBwdDeep>::smem_bytes<true>() <= 227 * 1024, "accumulators do not fit");
+static_assert(BwdShapeT<kBwdChunked>::smem_bytes<true>() <= 227 * 1024, "accumulators do not fit");
+static_assert(BwdShapeT<kBwdWide>::smem_bytes<false>() <= 227 * 1024, "ring and barriers do not fit");
 
 // hi + lo += v with the rounding error of hi + v carried into lo (the
 // two-sum of Knuth): summing n values keeps hi + lo within about
@@ -94,6 +104,11 @@ __device__ __forceinline__ void acc_two_sum(float& hi, float& lo, float v) {
     hi = s;
     lo = __fadd_rn(lo, e);
 }
+
+// Set when a kernel gave up waiting on a TMA tile (mbar_wait_bounded); the
+// outputs of that call are then incomplete. Never set in normal operation;
+// conv1d_wait_fault() reads it.
+__device__ int g_vcd_wait_fault = 0;
 
 constexpr int kPolicyBF16 = 0;
 constexpr int kPolicyFP32 = 1;
@@ -112,7 +127,8 @@ __device__ __forceinline__ float2 grad_at(float2 pre) {
 // a single unit, the unit-boundary logic compiles away, and the unit's
 // register sums are its row.
 template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG>
-__global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ BwdArgs a) {
     using SH = BwdShapeT<SHAPE>;
     constexpr int kBwdU = SH::kU, kBwdNs = SH::kNs;
     constexpr int kBwdTensorBytes = SH::kTensorBytes, kBwdStageBytes = SH::kStageBytes;
@@ -125,8 +141,10 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
     const int64_t nwarps = (int64_t)gridDim.x * SH::kWarps;
     const int64_t S = a.plan.S, C = a.plan.C, L = a.plan.L;
     const int64_t ncols = a.plan.ncols;
+#if !VCD_BWD_TMA
     const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(a.x);
     const __nv_bfloat16* __restrict__ dy = static_cast<const __nv_bfloat16*>(a.dy);
+#endif
     __nv_bfloat16* __restrict__ dx = static_cast<__nv_bfloat16*>(a.dx);
     const int32_t* __restrict__ cu = a.cu_seqlens;
     const int ncu = (int)(a.num_docs + 1);
@@ -144,6 +162,20 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
     const int64_t n_asg = ncols * a.plan.chunks;
     float* const acc = reinterpret_cast<float*>(smem + SH::kSmemBytes) +
                        wid * SH::kAccFloats * 32 + lane;        // SEG: [value][lane] of this warp
+    // TMA ring: this warp's stage barriers, initialised once (one arrival per
+    // phase: the producer lane's expect_tx); phase parities in `phases`.
+    const uint32_t bars = smem_u32(smem + SH::kSmemBytes + (SEG ? SH::kAccBytes : 0)) +
+                          wid * kBwdNs * 8;
+    uint32_t phases = 0;
+    bool fault = false;
+    if (VCD_BWD_TMA) {
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < kBwdNs; ++s) mbar_init(bars + 8 * s, 1);
+            mbar_init_fence();
+        }
+        __syncwarp();
+    }
     for (int64_t asg = warp0; asg < n_asg; asg += nwarps) {
         const int64_t col = asg % ncols, chunk = asg / ncols;
         const int64_t row0 = chunk * per;
@@ -165,21 +197,37 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
 
         // The first batches' copies go out before the taps and the document
         // lookup, whose dependent loads then overlap them.
+#if !VCD_BWD_TMA
         RowStream<2, kBwdRowBytes, int> rs;                 // x over [q0, u_end), dy over [t_begin, u_end)
         {
             const __nv_bfloat16* const bases[2] = {x, dy};
             const int64_t lows[2] = {q0 > 0 ? q0 : 0, t_begin};
             rs.init(bases, C, col, q0, lows, u_end, lane);
         }
+#endif
 
         __syncwarp();                    // the previous unit's reads of the ring are done
         auto issue = [&](int i, int slot) {
+#if VCD_BWD_TMA
+            // Tiles of tokens q0 + i U .. + U - 1 x the column's 128 channels
+            // (rows outside [0, S) and channels past C arrive as zeros; the
+            // x and dy rows outside what the unit uses are never read).
+            if (i < nb && lane == 0) {
+                const uint32_t st = ring_s + slot * kBwdStageBytes, bar = bars + 8 * slot;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, kBwdStageBytes);
+                const int c = (int)(col * kBwdColCh), t = (int)q0 + i * kBwdU;
+                tma_load_2d(st, &a.tmap_x, c, t, bar);
+                tma_load_2d(st + kBwdTensorBytes, &a.tmap_dy, c, t, bar);
+            }
+#else
             if (i < nb) {
                 const uint32_t st = ring_s + slot * kBwdStageBytes;
                 const uint32_t d[2] = {st, st + kBwdTensorBytes};
                 rs.stage<kBwdU>(d, i * kBwdU, x);
             }
             cp_async_commit();
+#endif
         };
 #pragma unroll
         for (int s = 0; s < kBwdNs - 1; ++s) issue(s, s);
@@ -261,7 +309,15 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
 
         int slot = 0;
         for (int i = 0; i < nb; ++i) {
+#if VCD_BWD_TMA
+            if (!mbar_wait_bounded(bars + 8 * slot, (phases >> slot) & 1u)) {
+                fault = true;
+                break;
+            }
+            phases ^= 1u << slot;
+#else
             cp_async_wait<kBwdNs - 2>();
+#endif
             __syncwarp();
             issue(i + kBwdNs - 1, slot == 0 ? kBwdNs - 1 : slot - 1);
             const int r0 = i * kBwdU;
@@ -413,7 +469,16 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1) bwd_main_kernel
             slot = slot + 1 == kBwdNs ? 0 : slot + 1;
         }
 
+        if (VCD_BWD_TMA && fault) break;
         write_row();
+    }
+    if (VCD_BWD_TMA && fault) {
+        // A tile never arrived: flag it, and give the stages still in flight
+        // a bounded wait of their own before the warp leaves, so that no copy
+        // lands in shared memory the CTA has released.
+        if (lane == 0) atomicExch(&g_vcd_wait_fault, 1);
+#pragma unroll
+        for (int s = 0; s < kBwdNs; ++s) mbar_wait_bounded(bars + 8 * s, (phases >> s) & 1u);
     }
     // Let the reduce kernel's CTAs be scheduled; its griddepcontrol.wait still
     // waits for this whole grid to finish and its writes to be visible.
@@ -532,7 +597,7 @@ int prepare_main_t() {
     // read the occupancy; both are host-side queries. The cache entries are
     // atomic (host threads may get here at once; each stores the same value).
     using SH = BwdShapeT<SHAPE>;
-    constexpr int kSmem = SEG ? SH::kSegSmemBytes : SH::kSmemBytes;
+    constexpr int kSmem = SH::template smem_bytes<SEG>();
     static std::atomic<int> occ[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
@@ -561,7 +626,7 @@ cudaError_t launch_main_form(const BwdArgs& a, int sm_count, cudaStream_t stream
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
     cfg.blockDim = dim3(SH::kThreads);
-    cfg.dynamicSmemBytes = SEG ? SH::kSegSmemBytes : SH::kSmemBytes;
+    cfg.dynamicSmemBytes = SH::template smem_bytes<SEG>();
     cfg.stream = stream;
     return cudaLaunchKernelEx(&cfg, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>, a);
 }
@@ -592,9 +657,66 @@ cudaError_t launch_reduce_t(const BwdArgs& a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, bwd_reduce_kernel<COMP>, a);
 }
 
+// cuTensorMapEncodeTiled from the driver (looked up once through the runtime,
+// so the library needs no link-time dependency on the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || p == nullptr)
+            return nullptr;
+        f = reinterpret_cast<EncodeTiledFn>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+// A [S, C] BF16 tensor as a 2D tensor map with boxes of `rows` tokens x one
+// 128-channel column (256 bytes a row); out-of-range elements read as zero.
+cudaError_t encode_rows(CUtensorMap* m, const void* base, int64_t S, int64_t C, int rows) {
+    EncodeTiledFn f = encode_tiled();
+    if (f == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)S};
+    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBwdColCh, (cuuint32_t)rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs& a, int sm_count, cudaStream_t stream) {
+// Reads (and clears) the flag a backward kernel sets when it gave up waiting
+// on a tile. Synchronous.
+cudaError_t read_wait_fault(int* flag) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(flag, g_vcd_wait_fault, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_vcd_wait_fault, &zero, sizeof(int));
+    return e;
+}
+
+cudaError_t launch_bwd(const BwdArgs& args, int sm_count, cudaStream_t stream) {
+    BwdArgs a = args;
+#if VCD_BWD_TMA
+    {
+        const int rows = a.shape == kBwdWide ? BwdGeom<kBwdWide>::kU
+                         : a.shape == kBwdDeep ? BwdGeom<kBwdDeep>::kU : BwdGeom<kBwdChunked>::kU;
+        cudaError_t e = encode_rows(&a.tmap_x, a.x, a.plan.S, a.plan.C, rows);
+        if (e == cudaSuccess) e = encode_rows(&a.tmap_dy, a.dy, a.plan.S, a.plan.C, rows);
+        if (e != cudaSuccess) return e;
+    }
+#endif
     typedef cudaError_t (*L)(const BwdArgs&, int, cudaStream_t);
 #define VCD_ROW(SH, WB, POL) {launch_main_t<SH, WB, kBiasNone, POL>, launch_main_t<SH, WB, kBiasF32, POL>, \
                               launch_main_t<SH, WB, kBiasBF16, POL>}

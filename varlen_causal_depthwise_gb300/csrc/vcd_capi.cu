@@ -193,6 +193,11 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* 
     return cuda_status(vcd::launch_bwd(a, sms, stream));
 }
 
+int conv1d_wait_fault(int* flag) {
+    if (!flag) return VCD_ERR_INVALID_ARG;
+    return cuda_status(vcd::read_wait_fault(flag));
+}
+
 const char* conv1d_status_string(int status) {
     switch (status) {
         case VCD_OK: return "ok";

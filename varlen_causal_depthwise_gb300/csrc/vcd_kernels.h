@@ -1,6 +1,7 @@
 // vcd_kernels.h -- argument blocks and launchers of the CUDA kernels; the C ABI
 // (vcd_capi.cu) validates arguments and calls these.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -42,6 +43,10 @@ struct BwdArgs {
     int dbias_bf16;
     int shape;                // BwdShape
     BwdPlan plan;             // bwd_plan(S, C, policy, shape)
+    // 2D tensor maps of x and dy ([S rows, C channels] BF16, boxes of the
+    // shape's batch of tokens x 128 channels), filled by launch_bwd.
+    CUtensorMap tmap_x;
+    CUtensorMap tmap_dy;
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, int sm_count, cudaStream_t stream);
@@ -53,5 +58,8 @@ int check_bwd_args(const void* x, const void* dy, int64_t S, int64_t C, const vo
                    int dweight_dtype, const void* dbias, int dbias_dtype);
 // Main kernel, then the reduce kernel launched programmatically dependent on it.
 cudaError_t launch_bwd(const BwdArgs& a, int sm_count, cudaStream_t stream);
+// The backward's wait-fault flag (set, never in normal operation, when a
+// kernel gave up waiting on a tile), read and cleared; synchronous.
+cudaError_t read_wait_fault(int* flag);
 
 }  // namespace vcd
