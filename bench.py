@@ -24,7 +24,8 @@ Printed JSON (one line, rank 0):
                own buffers: the forward's traffic (read x, write y) and the
                backward's (read x and dy, write dx) with no arithmetic.
   routes       every workload and SiLU' policy the operation is specified on,
-               forward and backward timed the same way (--no-sweep skips it).
+               forward and backward timed the same way, and the exactness-guarded
+               routes beside them (--no-sweep skips it).
   cpu_baseline the FP64 oracle (test infrastructure, single-threaded C) timed on
                a bounded slice of the same workload, and the same slice split
                by channels over every host core.
@@ -403,27 +404,40 @@ def sweep_leg(dev, iters, peak):
         dW = torch.empty(C, 4, dtype=w.weight.dtype, device=dev)
         dB = None if w.bias is None else torch.empty(C, dtype=w.bias.dtype, device=dev)
         fwd = lambda: vcd.conv1d_fwd(w.x, w.weight, w.cu_seqlens, w.bias, y=y, stream=stream)
+        fwd_x = lambda: vcd.conv1d_fwd_exact(w.x, w.weight, w.cu_seqlens, w.bias, y=y,
+                                             stream=stream)
         for _ in range(3):
             fwd()
+            fwd_x()
         f_us = time_events(fwd, iters, stream, flush if small else None)
+        fx_us = time_events(fwd_x, iters, stream, flush if small else None)
         fwd_b = 4 * S * C
+        wsx = torch.empty(vcd.conv1d_bwd_exact_workspace_size(S, C), dtype=torch.uint8, device=dev)
         for pol in recipe.policies:
             bwd = lambda: vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, pol, dx=dx,
                                          dweight=dW, dbias=dB, workspace=ws, stream=stream)
+            bwd_x = lambda: vcd.conv1d_bwd_exact(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, pol,
+                                                 dx=dx, dweight=dW, dbias=dB, workspace=wsx,
+                                                 stream=stream)
             for _ in range(3):
                 bwd()
+                bwd_x()
             b_us = time_events(bwd, iters, stream, flush if small else None)
+            bx_us = time_events(bwd_x, iters, stream, flush if small else None)
             bwd_b = compulsory_bytes(S, C, vcd_call_bytes(w, pol))[1]
             row = {"S": S, "C": C, "docs": w.num_docs, "policy": pol,
                    "l2": "flushed before each call" if small else "inputs larger than L2"}
-            for d, us, nb in (("fwd", f_us, fwd_b), ("bwd", b_us, bwd_b)):
+            # the exactness-guarded routes (conv1d_fwd_exact / conv1d_bwd_exact) moving
+            # the same compulsory bytes: their cost against the plain ones
+            for d, us, nb in (("fwd", f_us, fwd_b), ("bwd", b_us, bwd_b),
+                              ("fwd_exact", fx_us, fwd_b), ("bwd_exact", bx_us, bwd_b)):
                 gbs = nb / (us * 1e-6) / 1e9
                 row[d] = {"us_median": round(us, 2), "gbs": round(gbs, 1),
                           "frac_of_measured": round(gbs / peak, 4),
                           "frac_of_8tbs_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
                           "mtokens_per_s": round(S / (us * 1e-6) / 1e6, 2)}
             out[f"{name}/{pol}"] = row
-        del w, y, dx, ws
+        del w, y, dx, ws, wsx
         torch.cuda.empty_cache()
     return out
 

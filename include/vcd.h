@@ -114,6 +114,22 @@ int conv1d_fwd(const void* x, int64_t S, int64_t C,
                void* workspace, size_t workspace_bytes,
                cudaStream_t stream);
 
+/* Forward with every element of y within one BF16 ulp of the exact value
+ * (forward page, Returns: y = bf16(silu(...)), read as exact within one BF16
+ * ulp). Same arguments, checks and outputs as conv1d_fwd but no workspace.
+ * conv1d_fwd is within one ulp plus a first-order bound of FP32 rounding; it
+ * can miss the strict bound where the preactivation nearly cancels (|pre| well
+ * below the sum of its terms' magnitudes). This route checks each element
+ * against a bound of its FP32 error and recomputes the doubtful ones (a few
+ * in 10^4) from the exactly summed preactivation: slower than conv1d_fwd.
+ * Preactivations below -87.3, where SiLU's FP32 evaluation flushes to zero
+ * (|y| < 1.1e-36), keep that limit. */
+int conv1d_fwd_exact(const void* x, int64_t S, int64_t C,
+                     const void* weight, int weight_dtype,
+                     const int32_t* cu_seqlens, int64_t num_docs,
+                     const void* bias, int bias_dtype,
+                     void* y, cudaStream_t stream);
+
 /* Backward (backward page, description and Returns). Recomputes the FP32
  * preactivation from x, evaluates SiLU' at it per `policy`, and writes
  *   dx[t, c]      = bf16(sum_k weight[c, k] * dpre[t + 3 - k, c])  (same document)
@@ -150,6 +166,36 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C,
                void* dbias, int dbias_dtype,
                void* workspace, size_t workspace_bytes,
                cudaStream_t stream);
+
+/* Bytes of workspace conv1d_bwd_exact needs for (S, C), either policy: the
+ * partial rows of its launch shape, then per chunk of work a list of the dx
+ * elements to recompute (room for one in 256 elements) and its count. Errors
+ * as conv1d_bwd_workspace_size. */
+int conv1d_bwd_exact_workspace_size(int64_t S, int64_t C, size_t* bytes);
+
+/* Backward with every element of dx within one BF16 ulp of the exact value
+ * under the policy (backward page, Parameters: silu_grad_preactivation: dx is
+ * within one BF16 ulp of exact under both policies). Same arguments, checks
+ * and outputs as conv1d_bwd, with a workspace of
+ * conv1d_bwd_exact_workspace_size(S, C) bytes (no zeroing needed: every byte
+ * read is written first). conv1d_bwd is within one ulp plus a first-order
+ * bound of FP32 rounding; it can miss the strict bound where dx nearly
+ * cancels, or, under "bf16", where the FP32 preactivation and the exact one
+ * round to different BF16 values. This route takes the preactivations near a
+ * BF16 rounding midpoint from their exact sum, evaluates SiLU' to about
+ * 2^-22, bounds each dx's FP32 error, and recomputes in FP64 the few (a few
+ * in 10^4) that the bound cannot certify, in a third launch after the reduce.
+ * dweight and dbias are formed as in conv1d_bwd (same tolerances); under
+ * "bf16" they use the exactly rounded preactivations. Slower than conv1d_bwd. */
+int conv1d_bwd_exact(const void* x, const void* dy, int64_t S, int64_t C,
+                     const void* weight, int weight_dtype,
+                     const int32_t* cu_seqlens, int64_t num_docs,
+                     const void* bias, int bias_dtype,
+                     int policy,
+                     void* dx, void* dweight, int dweight_dtype,
+                     void* dbias, int dbias_dtype,
+                     void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
 
 /* Size of the fixed device scratch used by conv1d_bwd_noalloc: 8 MiB. Under
  * either policy that holds the partial rows of every shape with

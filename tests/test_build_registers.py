@@ -72,8 +72,9 @@ def _main_kernels(bwd):
 def test_forward_kernels_do_not_spill(resources):
     fwd, _ = resources
     kernels = {n: r for n, r in fwd.items() if "fwd_kernel" in n}
-    # per batch shape: 4 routes specialised on their dtypes, 1 taking them at run time
-    assert len(kernels) == 10
+    # per batch shape: 4 routes specialised on their dtypes, 1 taking them at run
+    # time; the exactness-guarded shape: the run-time route only
+    assert len(kernels) == 11
     for name, (regs, st, ld) in kernels.items():
         assert st == 0 and ld == 0, f"{name}: {regs} registers, spills {st}/{ld} bytes"
 
@@ -86,6 +87,12 @@ def test_backward_shapes_fit_their_register_budgets(resources):
     wide = {key: r for key, r in k.items() if key[0] == 0}
     deep = {key: r for key, r in k.items() if key[0] == 1}
     chunked = {key: r for key, r in k.items() if key[0] == 2}
+    # the exactness-guarded route: chunked shape, dtypes at run time (not in k,
+    # whose pattern matches the specialised routes), without spills
+    exact = {n: r for n, r in bwd.items() if "bwd_main_kernel" in n and "Lin1E" in n}
+    assert len(exact) == 3
+    for name, (regs, st, ld) in exact.items():
+        assert regs <= 168 and st == 0 and ld == 0, f"{name}: {regs} registers, spills {st}/{ld}"
     assert len(wide) == 4 and len(deep) == 6 and len(chunked) == 12
     assert all(key[3] == 0 and key[2] != 0 and key[4] == 0 for key in wide)
     assert all(key[3] == 0 and key[4] == 0 for key in deep)

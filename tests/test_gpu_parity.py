@@ -21,6 +21,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 REPORT = {}       # strict 1-ulp pass fractions
 REL_REPORT = {}   # rel-L2 of FP32 dweight / dbias
+EXACT_REPORT = {} # strict 1-ulp pass fractions of the exactness-guarded routes (all must be 1)
 
 
 def _np(t):
@@ -39,6 +40,13 @@ def run_bwd(w, policy, dweight_dtype=None, dbias_dtype=None, workspace=None):
         dB = torch.empty(C, dtype=dbias_dtype or w.bias.dtype, device=DEV)
     return vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, policy, dweight=dW,
                           dbias=dB, workspace=workspace)
+
+
+def run_bwd_exact(w, policy):
+    C = w.C
+    return vcd.conv1d_bwd_exact(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, policy,
+                                dweight=torch.empty(C, 4, device=DEV),
+                                dbias=None if w.bias is None else torch.empty(C, device=DEV))
 
 
 def run_grads(w, pol):
@@ -75,12 +83,20 @@ def full_check(wc, policies, what):
     torch.cuda.synchronize()
     ry, ay = oracle.fwd(wc.x, wc.weight, wc.cu_seqlens, wc.bias)
     REPORT[f"{what} y strict"] = bf16_close(_np(y), ry, ay, f"{what} y")
+    ye = vcd.conv1d_fwd_exact(w.x, w.weight, w.cu_seqlens, w.bias)
+    torch.cuda.synchronize()
+    EXACT_REPORT[f"{what} y"] = bf16_close(_np(ye), ry, None, f"{what} exact y", strict_miss_fraction=0)
     for pol in policies:
         rdx, adx, rdw, rdb = oracle.bwd(wc.x, wc.dy, wc.weight, wc.cu_seqlens, wc.bias, pol)
         dx, dW, dB, kw = run_grads(w, pol)
         torch.cuda.synchronize()
         REPORT[f"{what} {pol} dx strict"] = bf16_close(_np(dx), rdx, adx, f"{what} {pol} dx")
         check_grads(dW, dB, kw, rdw, rdb, pol, f"{what} {pol}")
+        dxe, dWe, dBe = run_bwd_exact(w, pol)
+        torch.cuda.synchronize()
+        EXACT_REPORT[f"{what} {pol} dx"] = bf16_close(_np(dxe), rdx, None, f"{what} {pol} exact dx",
+                                                      strict_miss_fraction=0)
+        grads_close(_np(dWe), None if dBe is None else _np(dBe), rdw, rdb, pol, f"{what} {pol} exact")
 
 
 # ------------------------------------------------------------- small, full --
@@ -221,7 +237,12 @@ def test_recipes_full_size_sampled(name):
     ry, ay = oracle.fwd_at(xc, wgt, cu, ts, cs, bias)
     yg = y[torch.from_numpy(ts).to(DEV), torch.from_numpy(cs).to(DEV)]
     REPORT[f"{name} full y strict"] = bf16_close(_np(yg), ry, ay, f"{name} y")
-    del y
+    ye = vcd.conv1d_fwd_exact(w.x, w.weight, w.cu_seqlens, w.bias, y=y)
+    torch.cuda.synchronize()
+    yeg = ye[torch.from_numpy(ts).to(DEV), torch.from_numpy(cs).to(DEV)]
+    EXACT_REPORT[f"{name} full y"] = bf16_close(_np(yeg), ry, None, f"{name} exact y",
+                                                strict_miss_fraction=0)
+    del y, ye
     chans = sample_channels(w.C, rng)
     for pol in synth.RECIPES[name].policies:
         dx, dW, dB, kw = run_grads(w, pol)
@@ -233,6 +254,18 @@ def test_recipes_full_size_sampled(name):
         del dx
         rdw, rdb = oracle.bwd_params_at(xc, dyc, wgt, cu, chans, bias, pol)
         check_grads(dW, dB, kw, rdw, rdb, pol, f"{name} full {pol}", chans)
+        del dW, dB, kw
+        dxe, dWe, dBe = run_bwd_exact(w, pol)
+        torch.cuda.synchronize()
+        dxeg = dxe[torch.from_numpy(ts).to(DEV), torch.from_numpy(cs).to(DEV)]
+        EXACT_REPORT[f"{name} full {pol} dx"] = bf16_close(_np(dxeg), rdx, None,
+                                                           f"{name} {pol} exact dx",
+                                                           strict_miss_fraction=0)
+        del dxe
+        errs = grads_close(_np(dWe)[chans], None if dBe is None else _np(dBe)[chans], rdw, rdb, pol,
+                           f"{name} full {pol} exact")
+        for k, v in errs.items():
+            REL_REPORT[f"{name} full {pol} exact {k}"] = v
     del w
     torch.cuda.empty_cache()
 
@@ -467,6 +500,8 @@ def test_report_accuracy(capsys):
         for k, v in sorted(REL_REPORT.items()):
             if " full " in k:
                 print(f"  rel-L2 {k}: {v:.3g}")
+        print(f"  exactness-guarded routes: {len(EXACT_REPORT)} cases, strict 1-ulp fraction "
+              f"{min(EXACT_REPORT.values()) if EXACT_REPORT else float('nan'):.6f} at worst")
 
 
 def test_no_tile_wait_gave_up():

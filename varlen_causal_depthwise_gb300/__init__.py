@@ -7,9 +7,10 @@ call does, and raises if the library has not been built.
 """
 from .binding import (  # noqa: F401
     VCD_OK, VCD_ERR_INVALID_ARG, VCD_ERR_WORKSPACE_TOO_SMALL, VCD_ERR_MISALIGNED, VCD_ERR_CUDA,
-    VcdError, conv1d_bwd, conv1d_bwd_call_workspace_size, conv1d_bwd_noalloc,
+    VcdError, conv1d_bwd, conv1d_bwd_call_workspace_size, conv1d_bwd_exact,
+    conv1d_bwd_exact_workspace_size, conv1d_bwd_noalloc,
     conv1d_bwd_route_workspace_size,
-    conv1d_bwd_workspace_size, conv1d_fwd, conv1d_fwd_workspace_size,
+    conv1d_bwd_workspace_size, conv1d_fwd, conv1d_fwd_exact, conv1d_fwd_workspace_size,
     conv1d_status_string, conv1d_wait_fault, library_path, load_library,
 )
 from .functional import (  # noqa: F401,E402

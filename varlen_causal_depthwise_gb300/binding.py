@@ -33,8 +33,12 @@ SIGNATURES = {
     "conv1d_bwd_call_workspace_size": (_int, [_i64, _i64, _i64, _int, _int, ctypes.POINTER(_sz)]),
     "conv1d_fwd": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _vp, _vp, _sz,
                           _vp]),
+    "conv1d_fwd_exact": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _vp, _vp]),
     "conv1d_bwd": (_int, [_vp, _vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _int, _vp,
                           _vp, _int, _vp, _int, _vp, _sz, _vp]),
+    "conv1d_bwd_exact_workspace_size": (_int, [_i64, _i64, ctypes.POINTER(_sz)]),
+    "conv1d_bwd_exact": (_int, [_vp, _vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _int, _vp,
+                                _vp, _int, _vp, _int, _vp, _sz, _vp]),
     "conv1d_bwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _vp, _int, _vp, _i64, _vp, _int, _int,
                                   _vp, _vp, _int, _vp, _int, _vp]),
     "conv1d_wait_fault": (_int, [ctypes.POINTER(_int)]),
@@ -187,8 +191,49 @@ def conv1d_fwd(x, weight, cu_seqlens, bias=None, y=None, workspace=None, stream=
     return y
 
 
+def conv1d_fwd_exact(x, weight, cu_seqlens, bias=None, y=None, stream=None):
+    """conv1d_fwd with every element of y within one BF16 ulp of the exact
+    value (the exactness-guarded route; slower). Same arguments."""
+    lib = load_library()
+    S, C = _sc(x)
+    dev = x.device
+    _require(x, "x", (torch.bfloat16,), dev)
+    _require(weight, "weight", (torch.float32, torch.bfloat16), dev, (C, 4))
+    _require(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
+    _require(bias, "bias", (torch.float32, torch.bfloat16), dev, (C,))
+    if y is None:
+        y = torch.empty_like(x)
+    _require(y, "y", (torch.bfloat16,), dev, x.shape)
+    with torch.cuda.device(dev):
+        st = lib.conv1d_fwd_exact(_ptr(x), S, C, _ptr(weight), _dt(weight), _ptr(cu_seqlens),
+                                  cu_seqlens.numel() - 1, _ptr(bias), _dt(bias), _ptr(y),
+                                  _stream(stream, dev))
+    _check(st, "conv1d_fwd_exact")
+    return y
+
+
+def conv1d_bwd_exact_workspace_size(S, C):
+    n = ctypes.c_size_t(0)
+    _check(load_library().conv1d_bwd_exact_workspace_size(int(S), int(C), ctypes.byref(n)),
+           "conv1d_bwd_exact_workspace_size")
+    return n.value
+
+
+def conv1d_bwd_exact(x, dy, weight, cu_seqlens, bias=None, policy="bf16", dx=None, dweight=None,
+                     dbias=None, workspace=None, stream=None, want_dbias=None):
+    """conv1d_bwd with every element of dx within one BF16 ulp of the exact
+    value (the exactness-guarded route; slower). Same arguments; the workspace
+    is conv1d_bwd_exact_workspace_size(S, C) bytes (allocated when omitted)."""
+    S, C = _sc(x)
+    if workspace is None:
+        workspace = torch.empty(conv1d_bwd_exact_workspace_size(S, C), dtype=torch.uint8,
+                                device=x.device)
+    return conv1d_bwd(x, dy, weight, cu_seqlens, bias, policy, dx, dweight, dbias, workspace,
+                      stream, want_dbias, _entry="conv1d_bwd_exact")
+
+
 def conv1d_bwd(x, dy, weight, cu_seqlens, bias=None, policy="bf16", dx=None, dweight=None,
-               dbias=None, workspace=None, stream=None, want_dbias=None):
+               dbias=None, workspace=None, stream=None, want_dbias=None, _entry="conv1d_bwd"):
     """Gradients of the forward: returns (dx, dweight, dbias or None).
 
     Output dtypes default to the parameters' dtypes. ``workspace`` (uint8, at
@@ -223,11 +268,12 @@ def conv1d_bwd(x, dy, weight, cu_seqlens, bias=None, policy="bf16", dx=None, dwe
     _require(workspace, "workspace", (torch.uint8,), dev)
     nbytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(dev):
-        st = lib.conv1d_bwd(_ptr(x), _ptr(dy), S, C, _ptr(weight), _dt(weight), _ptr(cu_seqlens),
-                            cu_seqlens.numel() - 1, _ptr(bias), _dt(bias), POLICIES[policy],
-                            _ptr(dx), _ptr(dweight), _dt(dweight), _ptr(dbias), _dt(dbias),
-                            _ptr(workspace), nbytes, _stream(stream, dev))
-    _check(st, "conv1d_bwd")
+        st = getattr(lib, _entry)(_ptr(x), _ptr(dy), S, C, _ptr(weight), _dt(weight),
+                                  _ptr(cu_seqlens), cu_seqlens.numel() - 1, _ptr(bias), _dt(bias),
+                                  POLICIES[policy], _ptr(dx), _ptr(dweight), _dt(dweight),
+                                  _ptr(dbias), _dt(dbias), _ptr(workspace), nbytes,
+                                  _stream(stream, dev))
+    _check(st, _entry)
     return dx, dweight, dbias
 
 

@@ -94,16 +94,7 @@ static_assert(BwdShapeT<kBwdDeep>::smem_bytes<true>() <= 227 * 1024, "accumulato
 static_assert(BwdShapeT<kBwdChunked>::smem_bytes<true>() <= 227 * 1024, "accumulators do not fit");
 static_assert(BwdShapeT<kBwdWide>::smem_bytes<false>() <= 227 * 1024, "ring and barriers do not fit");
 
-// hi + lo += v with the rounding error of hi + v carried into lo (the
-// two-sum of Knuth): summing n values keeps hi + lo within about
-// n 2^-48 of the exact sum relative to the sum of magnitudes.
-__device__ __forceinline__ void acc_two_sum(float& hi, float& lo, float v) {
-    const float s = __fadd_rn(hi, v);
-    const float bv = __fsub_rn(s, hi);
-    const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bv)), __fsub_rn(v, bv));
-    hi = s;
-    lo = __fadd_rn(lo, e);
-}
+
 
 // Set when a kernel gave up waiting on a TMA tile (mbar_wait_bounded); the
 // outputs of that call are then incomplete. Never set in normal operation;
@@ -126,7 +117,13 @@ __device__ __forceinline__ float2 grad_at(float2 pre) {
 // unit boundary; the chunk writes one partial row. Without SEG every chunk is
 // a single unit, the unit-boundary logic compiles away, and the unit's
 // register sums are its row.
-template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG>
+// EXACT: the exactness-guarded route (conv1d_bwd_exact), every batch through
+// one predicated path with checks (below); instantiated with BIAS =
+// kRouteRuntime (dtypes read at run time).
+constexpr float kU24 = 0x1p-24f;                  // FP32 unit roundoff
+constexpr float kExactScale = 0x1p-11f;           // magnitudes are kept scaled by this
+
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG, bool EXACT = false>
 __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdArgs a) {
     using SH = BwdShapeT<SHAPE>;
@@ -149,6 +146,7 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
     const int32_t* __restrict__ cu = a.cu_seqlens;
     const int ncu = (int)(a.num_docs + 1);
     const int Ci = (int)C;                               // row stride, elements
+    const bool with_bias = BIAS == kRouteRuntime ? a.bias_kind != kBiasNone : BIAS != kBiasNone;
 
     // Assignment. Each column's units are cut into chunks of `per` consecutive
     // units (the plan's, from constants), and a warp streams a whole chunk as
@@ -233,17 +231,23 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
         for (int s = 0; s < kBwdNs - 1; ++s) issue(s, s);
 
         float2 w[4][kNP], b[kNP];
-        load_taps<W_BF16, BIAS, kNP>(a.weight, a.bias, c0, active, w, b);
+        if constexpr (BIAS == kRouteRuntime)
+            load_taps_rt(a.weight, a.bias, a.weight_bf16 != 0, a.bias_kind, c0, active, w, b);
+        else
+            load_taps<W_BF16, BIAS, kNP>(a.weight, a.bias, c0, active, w, b);
         DocCursor doc;
         doc.init(cu, ncu, (int)q0 - 2, lane);
         uint32_t carry = doc.starts(cu, ncu, (int)q0 - 2, 2, lane);            // bits of q0-2, q0-1
 
         float2 xc[3][kNP], dc[3][kNP];    // x and dpre of tokens q-3, q-2, q-1
         float2 dw[4][kNP], db[kNP];       // this unit's FP32 sums
+        float2 ec[3][kNP];                // EXACT: bounds on the error of those dpre
+        uint32_t xn = 0;                  // EXACT: this chunk's listed elements (warp-uniform)
+        uint64_t* const xlist = EXACT ? a.xlist + asg * a.xcap : nullptr;
 #pragma unroll
         for (int p = 0; p < kNP; ++p) {
 #pragma unroll
-            for (int k = 0; k < 3; ++k) xc[k][p] = dc[k][p] = zero2();
+            for (int k = 0; k < 3; ++k) xc[k][p] = dc[k][p] = ec[k][p] = zero2();
 #pragma unroll
             for (int k = 0; k < 4; ++k) dw[k][p] = zero2();
             db[p] = zero2();
@@ -295,12 +299,146 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
                 }
             }
             if (!SEG) clear_sums();
+            if (EXACT && lane == 0) a.xcount[asg] = xn;
         };
         // SEG: token r (at position 3 of its batch) starts the next unit.
         auto unit_boundary = [&](int r) {
             if (SEG && r == r_next) {
                 fold_unit();
                 r_next = r_next + Li < r_end ? r_next + Li : INT_MAX;
+            }
+        };
+
+        // EXACT: one token of the guarded route. As the general path, plus:
+        //  - "bf16" policy: a preactivation within its FP32 error bound
+        //    (4 2^-24 mag, mag = the magnitude of its terms) of a BF16
+        //    rounding midpoint is summed exactly before it is rounded, so p
+        //    is the rounding of the exact preactivation;
+        //  - SiLU' by the accurate evaluation for both policies;
+        //  - a bound on each dpre's error (e: SiLU' evaluation (16 + 16|p|)
+        //    2^-24 times |dy|, the product's rounding, and under "fp32" the
+        //    preactivation's error times max|silu''| = 1/2) and on dx's:
+        //    sum |w| e + 5 2^-24 sum |w dpre|. A dx whose bound exceeds 2^-10
+        //    of its value goes to the chunk's list (its BF16 rounding might
+        //    miss the 1-ulp bound) and is recomputed in FP64 afterwards.
+        auto exact_token = [&](int r, const uint32_t (&xv)[kNP], const uint32_t (&gv)[kNP], bool m1,
+                               bool m2, bool m3, bool k1, bool k2, bool k3, bool has_d, bool acc,
+                               bool emit, uint32_t (&o)[kNP]) {
+            float2 pre[kNP], mag[kNP], xf[kNP], gf[kNP];
+            uint32_t flip = 0;                       // bit 2p + h: preactivation needs its exact sum
+#pragma unroll
+            for (int p = 0; p < kNP; ++p) {
+                xf[p] = bf16x2_to_float2(xv[p]);
+                gf[p] = bf16x2_to_float2(gv[p]);
+                const float2 xs[4] = {xc[0][p], xc[1][p], xc[2][p], xf[p]};
+                const bool on[4] = {m3, m2, m1, true};
+                pre[p] = b[p];
+                mag[p] = make_float2(fabsf(b[p].x) * kExactScale, fabsf(b[p].y) * kExactScale);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (!on[k]) continue;
+                    pre[p] = fma2<false>(w[k][p], xs[k], pre[p]);
+                    mag[p].x = __fmaf_rn(fabsf(w[k][p].x) * kExactScale, fabsf(xs[k].x), mag[p].x);
+                    mag[p].y = __fmaf_rn(fabsf(w[k][p].y) * kExactScale, fabsf(xs[k].y), mag[p].y);
+                }
+                if (POLICY == kPolicyBF16 && has_d) {
+                    // |pre - midpoint of its BF16 interval| (exact: Sterbenz) vs 4 2^-24 mag
+                    const float e_pre[2] = {mag[p].x * kExactScale, mag[p].y * kExactScale};
+                    const float pv[2] = {pre[p].x, pre[p].y};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float mid = __uint_as_float((__float_as_uint(pv[h]) & 0xffff0000u) | 0x8000u);
+                        if (fabsf(__fsub_rn(pv[h], mid)) <= e_pre[h]) flip |= 1u << (2 * p + h);
+                    }
+                }
+            }
+            float2 pt[kNP];                           // the point SiLU' is taken at
+#pragma unroll
+            for (int p = 0; p < kNP; ++p) pt[p] = POLICY == kPolicyBF16 ? round_bf16x2(pre[p]) : pre[p];
+            if (POLICY == kPolicyBF16 && __any_sync(kFull, flip != 0)) {
+#pragma unroll
+                for (int e = 0; e < 2 * kNP; ++e) {
+                    if (!((flip >> e) & 1u)) continue;
+                    const int p = e >> 1;
+                    const bool hi = e & 1;
+                    const float wk[4] = {hi ? w[0][p].y : w[0][p].x, hi ? w[1][p].y : w[1][p].x,
+                                         hi ? w[2][p].y : w[2][p].x, hi ? w[3][p].y : w[3][p].x};
+                    const float xk[4] = {hi ? xc[0][p].y : xc[0][p].x, hi ? xc[1][p].y : xc[1][p].x,
+                                         hi ? xc[2][p].y : xc[2][p].x, hi ? xf[p].y : xf[p].x};
+                    const bool on[4] = {m3, m2, m1, true};
+                    const double pe = exact_preactivation(hi ? b[p].y : b[p].x, wk, xk, on);
+                    const float pr = __bfloat162float(__double2bfloat16(pe));
+                    if (hi) pt[p].y = pr; else pt[p].x = pr;
+                }
+            }
+            uint32_t doubt = 0;                       // bit 2p + h: dx of channel 2p + h is listed
+#pragma unroll
+            for (int p = 0; p < kNP; ++p) {
+                float2 d = zero2(), ed = zero2();
+                if (has_d) {
+                    const float2 g = silu_grad2_accurate(pt[p]);
+                    d = mul2<false>(gf[p], g);
+                    const float2 eg = make_float2(kU24 * (16.0f + 16.0f * fabsf(pt[p].x)),
+                                                  kU24 * (16.0f + 16.0f * fabsf(pt[p].y)));
+                    ed.x = __fmaf_rn(fabsf(gf[p].x), eg.x, kU24 * fabsf(d.x));
+                    ed.y = __fmaf_rn(fabsf(gf[p].y), eg.y, kU24 * fabsf(d.y));
+                    if (POLICY == kPolicyFP32) {          // |silu''| <= 1/2 times 4 2^-24 mag
+                        ed.x = __fmaf_rn(fabsf(gf[p].x), mag[p].x * (0.5f * kExactScale), ed.x);
+                        ed.y = __fmaf_rn(fabsf(gf[p].y), mag[p].y * (0.5f * kExactScale), ed.y);
+                    }
+                }
+                if (acc) {
+                    if (m3) dw[0][p] = fma2<kPA>(d, xc[0][p], dw[0][p]);
+                    if (m2) dw[1][p] = fma2<kPA>(d, xc[1][p], dw[1][p]);
+                    if (m1) dw[2][p] = fma2<kPA>(d, xc[2][p], dw[2][p]);
+                    dw[3][p] = fma2<kPA>(d, xf[p], dw[3][p]);
+                    if (with_bias) db[p] = add2<kPA>(db[p], d);
+                }
+                float2 g = mul2<kPA>(w[3][p], dc[0][p]);
+                if (k1) g = fma2<kPA>(w[2][p], dc[1][p], g);
+                if (k2) g = fma2<kPA>(w[1][p], dc[2][p], g);
+                if (k3) g = fma2<kPA>(w[0][p], d, g);
+                o[p] = float2_to_bf16x2(g);
+                // error bound of this dx: the dpre errors carried by |w|, and
+                // 5 roundings' worth of the terms' magnitude
+                const float2 ds[4] = {dc[0][p], dc[1][p], dc[2][p], d};
+                const float2 es[4] = {ec[0][p], ec[1][p], ec[2][p], ed};
+                const bool in[4] = {true, k1, k2, k3};
+                const int tap[4] = {3, 2, 1, 0};
+                float ex = 0.0f, ey = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (!in[i]) continue;
+                    const float2 aw = make_float2(fabsf(w[tap[i]][p].x), fabsf(w[tap[i]][p].y));
+                    ex = __fmaf_rn(aw.x, __fmaf_rn(5.0f * kU24, fabsf(ds[i].x), es[i].x), ex);
+                    ey = __fmaf_rn(aw.y, __fmaf_rn(5.0f * kU24, fabsf(ds[i].y), es[i].y), ey);
+                }
+                if (emit && ex > 0x1p-10f * fabsf(g.x)) doubt |= 1u << (2 * p);
+                if (emit && ey > 0x1p-10f * fabsf(g.y)) doubt |= 2u << (2 * p);
+                xc[0][p] = xc[1][p];
+                xc[1][p] = xc[2][p];
+                xc[2][p] = xf[p];
+                dc[0][p] = dc[1][p];
+                dc[1][p] = dc[2][p];
+                dc[2][p] = d;
+                ec[0][p] = ec[1][p];
+                ec[1][p] = ec[2][p];
+                ec[2][p] = ed;
+            }
+            if (__any_sync(kFull, doubt != 0)) {
+                // list dx[t - 3] of the doubtful channels, warp-aggregated
+                const uint32_t below = (1u << lane) - 1u;
+                const uint64_t t3 = (uint64_t)(q0 + r - 3);      // the token whose dx this is
+#pragma unroll
+                for (int e = 0; e < 2 * kNP; ++e) {
+                    const bool mine = (doubt >> e) & 1u;
+                    const uint32_t bal = __ballot_sync(kFull, mine);
+                    if (bal == 0) continue;
+                    const uint32_t pos = xn + __popc(bal & below);
+                    if (mine && pos < (uint32_t)a.xcap)
+                        xlist[pos] = (t3 << 32) | (uint64_t)(c0 + e);
+                    xn += __popc(bal);
+                }
             }
         };
 
@@ -332,7 +470,27 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
             // an interior batch: every token accumulates and emits dx three
             // tokens back (a unit boundary, if any, is at position 3)
             const bool interior = r0 >= 6 && r0 + kBwdU <= r_end;
-            if (M == 0 && interior) {
+            if constexpr (EXACT) {
+#pragma unroll
+                for (int j = 0; j < kBwdU; ++j) {
+                    const int r = r0 + j;
+                    if (j == 3) unit_boundary(r);
+                    uint32_t xv[kNP], gv[kNP], o[kNP];
+                    lds_pairs<kBwdVec>(sx + j * kBwdRowBytes, xv);
+                    lds_pairs<kBwdVec>(sg + j * kBwdRowBytes, gv);
+                    const bool m1 = !bit(M, j + 2);
+                    const bool m2 = m1 && !bit(M, j + 1);
+                    const bool m3 = m2 && !bit(M, j);
+                    const bool k1 = !bit(M, j);
+                    const bool k2 = k1 && !bit(M, j + 1);
+                    const bool k3 = k2 && !bit(M, j + 2);
+                    const bool has_d = r >= 3 && r < r_du;
+                    const bool acc = r >= 3 && r < r_end;
+                    const bool emit = active && r >= 6 && r - 3 < r_end;
+                    exact_token(r, xv, gv, m1, m2, m3, k1, k2, k3, has_d, acc, emit, o);
+                    if (emit) st_pairs<kBwdVec>(dxq + j * Ci, o);
+                }
+            } else if (M == 0 && interior) {
 #pragma unroll
                 for (int j = 0; j < kBwdU; ++j) {
                     if (j == 3) unit_boundary(r0 + j);
@@ -352,7 +510,7 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
                         dw[1][p] = fma2<kPA>(d, xc[1][p], dw[1][p]);
                         dw[2][p] = fma2<kPA>(d, xc[2][p], dw[2][p]);
                         dw[3][p] = fma2<kPA>(d, xf, dw[3][p]);
-                        if (BIAS != kBiasNone) db[p] = add2<kPA>(db[p], d);
+                        if (with_bias) db[p] = add2<kPA>(db[p], d);
                         float2 g = mul2<kPA>(w[3][p], dc[0][p]);
                         g = fma2<kPA>(w[2][p], dc[1][p], g);
                         g = fma2<kPA>(w[1][p], dc[2][p], g);
@@ -399,7 +557,7 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
                         if (m2) dw[1][p] = fma2<kPA>(d, xc[1][p], dw[1][p]);
                         if (m1) dw[2][p] = fma2<kPA>(d, xc[2][p], dw[2][p]);
                         dw[3][p] = fma2<kPA>(d, xf, dw[3][p]);
-                        if (BIAS != kBiasNone) db[p] = add2<kPA>(db[p], d);
+                        if (with_bias) db[p] = add2<kPA>(db[p], d);
                         float2 g = mul2<kPA>(w[3][p], dc[0][p]);
                         if (k1) g = fma2<kPA>(w[2][p], dc[1][p], g);
                         if (k2) g = fma2<kPA>(w[1][p], dc[2][p], g);
@@ -449,7 +607,7 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
                             if (m2) dw[1][p] = fma2<kPA>(d, xc[1][p], dw[1][p]);
                             if (m1) dw[2][p] = fma2<kPA>(d, xc[2][p], dw[2][p]);
                             dw[3][p] = fma2<kPA>(d, xf, dw[3][p]);
-                            if (BIAS != kBiasNone) db[p] = add2<kPA>(db[p], d);
+                            if (with_bias) db[p] = add2<kPA>(db[p], d);
                         }
                         float2 g = mul2<kPA>(w[3][p], dc[0][p]);
                         if (k1) g = fma2<kPA>(w[2][p], dc[1][p], g);
@@ -589,9 +747,105 @@ __global__ void __launch_bounds__(kRedOutputs * kRedMaxSlices, 4) bwd_reduce_ker
     }
 }
 
+// ------------------------------------------------------- exact fix-up ---
+
+// First token of the document holding t (the last cu_seqlens entry <= t);
+// clamped so that a malformed array cannot send a read out of range.
+__device__ int64_t doc_start_of(const int32_t* __restrict__ cu, int ncu, int64_t t) {
+    int lo = 0, hi = ncu;                                   // cu[lo] <= t < cu[hi] when sorted
+    while (hi - lo > 1) {
+        const int mid = lo + (hi - lo) / 2;
+        if ((int64_t)__ldg(cu + mid) <= t) lo = mid; else hi = mid;
+    }
+    const int64_t s = __ldg(cu + lo);
+    return s < 0 ? 0 : s > t ? t : s;
+}
+
+__device__ double param_at(const void* base, bool bf16, int64_t i) {
+    if (bf16) return (double)__bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
+    return (double)reinterpret_cast<const float*>(base)[i];
+}
+
+// sigmoid(p) for either sign without overflow.
+__device__ double sigmoid64(double p) {
+    if (p >= 0.0) return 1.0 / (1.0 + exp(-p));
+    const double e = exp(p);
+    return e / (1.0 + e);
+}
+
+// dx[t, c] of the policy in FP64 from the inputs: each preactivation summed
+// exactly (the products of FP32 or BF16 weights and BF16 inputs are exact in
+// FP64; compensated sums), SiLU' at the policy's point, and the four-term sum,
+// rounded once to BF16.
+__device__ __nv_bfloat16 dx_exact(const BwdArgs& a, int64_t t, int64_t c) {
+    const int64_t S = a.plan.S, C = a.plan.C;
+    const int32_t* cu = a.cu_seqlens;
+    const int ncu = (int)(a.num_docs + 1);
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+    const __nv_bfloat16* dy = static_cast<const __nv_bfloat16*>(a.dy);
+    const bool wb = a.weight_bf16 != 0;
+    double wk[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) wk[k] = param_at(a.weight, wb, c * 4 + k);
+    const double bias = a.bias_kind == kBiasNone ? 0.0 : param_at(a.bias, a.bias_kind == kBiasBF16, c);
+    const int64_t s0 = doc_start_of(cu, ncu, t);
+    double sum = 0.0, comp = 0.0;
+    for (int k = 0; k < 4; ++k) {
+        const int64_t j = t + 3 - k;                         // the token whose pre used x[t] via tap k
+        if (j >= S || doc_start_of(cu, ncu, j) != s0) continue;
+        double pre = bias, pc = 0.0;
+        for (int m = 0; m < 4; ++m) {
+            const int64_t i = j - 3 + m;
+            if (i < s0) continue;
+            const double v = wk[m] * (double)__bfloat162float(x[i * C + c]);
+            const double u = pre + v;
+            pc += fabs(pre) >= fabs(v) ? (pre - u) + v : (v - u) + pre;
+            pre = u;
+        }
+        pre += pc;
+        const double p = a.policy == kPolicyBF16 ? (double)__bfloat162float(__double2bfloat16(pre)) : pre;
+        const double g = sigmoid64(p) * (1.0 + p * sigmoid64(-p));
+        const double term = wk[k] * ((double)__bfloat162float(dy[j * C + c]) * g);
+        const double u = sum + term;
+        comp += fabs(sum) >= fabs(term) ? (sum - u) + term : (term - u) + sum;
+        sum = u;
+    }
+    return __double2bfloat16(sum + comp);
+}
+
+// Recomputes the dx elements the guarded main kernel listed, one list (one
+// chunk of one column) per CTA; a list that overflowed its room means every
+// element of its chunk.
+__global__ void __launch_bounds__(256) bwd_exact_fixup_kernel(const BwdArgs a) {
+    const BwdPlan& P = a.plan;
+    const int64_t lists = P.ncols * P.chunks;
+    __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(a.dx);
+    for (int64_t id = blockIdx.x; id < lists; id += gridDim.x) {
+        const uint32_t n = a.xcount[id];
+        if (n <= (uint64_t)a.xcap) {
+            const uint64_t* list = a.xlist + id * a.xcap;
+            for (uint32_t e = threadIdx.x; e < n; e += blockDim.x) {
+                const uint64_t v = list[e];
+                const int64_t t = (int64_t)(v >> 32), c = (int64_t)(v & 0xffffffffu);
+                if (t < P.S && c < P.C) dx[t * P.C + c] = dx_exact(a, t, c);
+            }
+        } else {
+            const int64_t col = id % P.ncols, chunk = id / P.ncols;
+            const int64_t r0 = chunk * P.per, r1 = r0 + P.per < P.rows ? r0 + P.per : P.rows;
+            const int64_t t0 = r0 * P.L, t1 = r1 * P.L < P.S ? r1 * P.L : P.S;
+            const int64_t c0 = col * kBwdColCh;
+            const int64_t nc = P.C - c0 < kBwdColCh ? P.C - c0 : kBwdColCh;
+            for (int64_t e = threadIdx.x; e < (t1 - t0) * nc; e += blockDim.x) {
+                const int64_t t = t0 + e / nc, c = c0 + e % nc;
+                dx[t * P.C + c] = dx_exact(a, t, c);
+            }
+        }
+    }
+}
+
 // -------------------------------------------------------------- launch ---
 
-template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG>
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG, bool EXACT = false>
 int prepare_main_t() {
     // Once per (instantiation, device): allow the dynamic shared memory and
     // read the occupancy; both are host-side queries. The cache entries are
@@ -603,21 +857,21 @@ int prepare_main_t() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     const int known = occ[dev].load(std::memory_order_relaxed);
     if (known > 0) return known;
-    if (cudaFuncSetAttribute(bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>,
+    if (cudaFuncSetAttribute(bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT>,
                                                       SH::kThreads, kSmem) != cudaSuccess)
         return 0;
     occ[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
-template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG>
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG, bool EXACT = false>
 cudaError_t launch_main_form(const BwdArgs& a, int sm_count, cudaStream_t stream) {
     using SH = BwdShapeT<SHAPE>;
-    const int occ = prepare_main_t<SHAPE, W_BF16, BIAS, POLICY, SEG>();
+    const int occ = prepare_main_t<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT>();
     if (occ <= 0) return cudaErrorInvalidConfiguration;
     const int64_t n_asg = a.plan.ncols * a.plan.chunks;
     const int64_t ctas_needed = (n_asg + SH::kWarps - 1) / SH::kWarps;
@@ -628,7 +882,7 @@ cudaError_t launch_main_form(const BwdArgs& a, int sm_count, cudaStream_t stream
     cfg.blockDim = dim3(SH::kThreads);
     cfg.dynamicSmemBytes = SH::template smem_bytes<SEG>();
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG>, a);
+    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT>, a);
 }
 
 // Chunks of several units come only from the "fp32" policy, which runs the
@@ -680,22 +934,21 @@ EncodeTiledFn encode_tiled() {
     return f;
 }
 
-// A [S, C] BF16 tensor as a 2D tensor map with boxes of `rows` tokens x one
-// 128-channel column (256 bytes a row); out-of-range elements read as zero.
-cudaError_t encode_rows(CUtensorMap* m, const void* base, int64_t S, int64_t C, int rows) {
+}  // namespace
+
+cudaError_t encode_bf16_rows(CUtensorMap* m, const void* base, int64_t S, int64_t C, int cols,
+                             int rows) {
     EncodeTiledFn f = encode_tiled();
     if (f == nullptr) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)S};
     const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBwdColCh, (cuuint32_t)rows};
+    const cuuint32_t box[2] = {(cuuint32_t)cols, (cuuint32_t)rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-
-}  // namespace
 
 // Reads (and clears) the flag a backward kernel sets when it gave up waiting
 // on a tile. Synchronous.
@@ -706,17 +959,49 @@ cudaError_t read_wait_fault(int* flag) {
     return e;
 }
 
+namespace {
+cudaError_t encode_maps(BwdArgs& a) {
+#if VCD_BWD_TMA
+    const int rows = a.shape == kBwdWide ? BwdGeom<kBwdWide>::kU
+                     : a.shape == kBwdDeep ? BwdGeom<kBwdDeep>::kU : BwdGeom<kBwdChunked>::kU;
+    cudaError_t e = encode_bf16_rows(&a.tmap_x, a.x, a.plan.S, a.plan.C, kBwdColCh, rows);
+    if (e == cudaSuccess) e = encode_bf16_rows(&a.tmap_dy, a.dy, a.plan.S, a.plan.C, kBwdColCh, rows);
+    return e;
+#else
+    (void)a;
+    return cudaSuccess;
+#endif
+}
+}  // namespace
+
+cudaError_t launch_bwd_exact(const BwdArgs& args, int sm_count, cudaStream_t stream) {
+    BwdArgs a = args;
+    cudaError_t e = encode_maps(a);
+    if (e != cudaSuccess) return e;
+    const bool fp32 = a.policy == kPolicyFP32;
+    if (fp32 && a.plan.per > 1)
+        e = launch_main_form<kBwdChunked, false, kRouteRuntime, kPolicyFP32, true, true>(a, sm_count, stream);
+    else if (fp32)
+        e = launch_main_form<kBwdChunked, false, kRouteRuntime, kPolicyFP32, false, true>(a, sm_count, stream);
+    else if (a.plan.per == 1)
+        e = launch_main_form<kBwdChunked, false, kRouteRuntime, kPolicyBF16, false, true>(a, sm_count, stream);
+    else
+        e = cudaErrorInvalidValue;
+    if (e != cudaSuccess) return e;
+    e = fp32 ? launch_reduce_t<true>(a, stream) : launch_reduce_t<false>(a, stream);
+    if (e != cudaSuccess) return e;
+    const int64_t lists = a.plan.ncols * a.plan.chunks;
+    const int64_t grid = lists < (int64_t)sm_count * 8 ? lists : (int64_t)sm_count * 8;
+    bwd_exact_fixup_kernel<<<(unsigned)(grid > 0 ? grid : 1), 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd(const BwdArgs& args, int sm_count, cudaStream_t stream) {
     BwdArgs a = args;
-#if VCD_BWD_TMA
     {
-        const int rows = a.shape == kBwdWide ? BwdGeom<kBwdWide>::kU
-                         : a.shape == kBwdDeep ? BwdGeom<kBwdDeep>::kU : BwdGeom<kBwdChunked>::kU;
-        cudaError_t e = encode_rows(&a.tmap_x, a.x, a.plan.S, a.plan.C, rows);
-        if (e == cudaSuccess) e = encode_rows(&a.tmap_dy, a.dy, a.plan.S, a.plan.C, rows);
+        const cudaError_t e = encode_maps(a);
         if (e != cudaSuccess) return e;
     }
-#endif
     typedef cudaError_t (*L)(const BwdArgs&, int, cudaStream_t);
 #define VCD_ROW(SH, WB, POL) {launch_main_t<SH, WB, kBiasNone, POL>, launch_main_t<SH, WB, kBiasF32, POL>, \
                               launch_main_t<SH, WB, kBiasBF16, POL>}

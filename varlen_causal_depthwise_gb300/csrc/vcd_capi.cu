@@ -119,11 +119,14 @@ int conv1d_bwd_call_workspace_size(int64_t S, int64_t C, int64_t num_docs, int p
     return VCD_OK;
 }
 
-int conv1d_fwd(const void* x, int64_t S, int64_t C, const void* weight, int weight_dtype,
-               const int32_t* cu_seqlens, int64_t num_docs, const void* bias, int bias_dtype,
-               void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
+}  // extern "C"
+
+namespace {
+
+// conv1d_fwd and conv1d_fwd_exact: the same checks, then the route.
+int fwd_call(const void* x, int64_t S, int64_t C, const void* weight, int weight_dtype,
+             const int32_t* cu_seqlens, int64_t num_docs, const void* bias, int bias_dtype,
+             void* y, cudaStream_t stream, bool exact) {
     int st = check_shape(S, C, num_docs);
     if (st != VCD_OK) return st;
     if (!dtype_ok(weight_dtype) || (bias && !dtype_ok(bias_dtype))) return VCD_ERR_INVALID_ARG;
@@ -146,14 +149,45 @@ int conv1d_fwd(const void* x, int64_t S, int64_t C, const void* weight, int weig
     a.weight_bf16 = weight_dtype == VCD_BF16;
     a.bias_kind = !bias ? vcd::kBiasNone : bias_dtype == VCD_BF16 ? vcd::kBiasBF16 : vcd::kBiasF32;
     a.plan = vcd::fwd_plan(S, C);
-    return cuda_status(vcd::launch_fwd(a, sms, stream));
+    return cuda_status(exact ? vcd::launch_fwd_exact(a, sms, stream) : vcd::launch_fwd(a, sms, stream));
 }
 
-int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* weight,
-               int weight_dtype, const int32_t* cu_seqlens, int64_t num_docs, const void* bias,
-               int bias_dtype, int policy, void* dx, void* dweight, int dweight_dtype,
-               void* dbias, int dbias_dtype, void* workspace, size_t workspace_bytes,
-               cudaStream_t stream) {
+}  // namespace
+
+extern "C" {
+
+int conv1d_fwd(const void* x, int64_t S, int64_t C, const void* weight, int weight_dtype,
+               const int32_t* cu_seqlens, int64_t num_docs, const void* bias, int bias_dtype,
+               void* y, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    return fwd_call(x, S, C, weight, weight_dtype, cu_seqlens, num_docs, bias, bias_dtype, y, stream,
+                    false);
+}
+
+int conv1d_fwd_exact(const void* x, int64_t S, int64_t C, const void* weight, int weight_dtype,
+                     const int32_t* cu_seqlens, int64_t num_docs, const void* bias, int bias_dtype,
+                     void* y, cudaStream_t stream) {
+    return fwd_call(x, S, C, weight, weight_dtype, cu_seqlens, num_docs, bias, bias_dtype, y, stream,
+                    true);
+}
+
+int conv1d_bwd_exact_workspace_size(int64_t S, int64_t C, size_t* bytes) {
+    if (!bytes || check_shape(S, C, S > 0 ? 1 : 0) != VCD_OK) return VCD_ERR_INVALID_ARG;
+    *bytes = (size_t)vcd::bwd_exact_workspace_bytes(S, C);
+    return VCD_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// conv1d_bwd and conv1d_bwd_exact: the same checks, then the route.
+int bwd_call(const void* x, const void* dy, int64_t S, int64_t C, const void* weight,
+             int weight_dtype, const int32_t* cu_seqlens, int64_t num_docs, const void* bias,
+             int bias_dtype, int policy, void* dx, void* dweight, int dweight_dtype, void* dbias,
+             int dbias_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+             bool exact) {
     int st = vcd::check_bwd_args(x, dy, S, C, weight, weight_dtype, cu_seqlens, num_docs, bias,
                                  bias_dtype, policy, dx, dweight, dweight_dtype, dbias, dbias_dtype);
     if (st != VCD_OK) return st;
@@ -165,8 +199,9 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* 
     }
     const int weight_bf16 = weight_dtype == VCD_BF16;
     const int bias_kind = !bias ? vcd::kBiasNone : bias_dtype == VCD_BF16 ? vcd::kBiasBF16 : vcd::kBiasF32;
-    const int shape = vcd::bwd_shape(S, num_docs, policy, bias != nullptr);
-    const uint64_t need = vcd::bwd_workspace_bytes_for(S, C, policy, shape);   // this route's rows
+    const int shape = exact ? vcd::kBwdChunked : vcd::bwd_shape(S, num_docs, policy, bias != nullptr);
+    const vcd::ExactLayout xl = vcd::exact_layout(S, C, policy);
+    const uint64_t need = exact ? xl.total : vcd::bwd_workspace_bytes_for(S, C, policy, shape);
     if (!workspace || workspace_bytes < need) return VCD_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned(workspace, 16)) return VCD_ERR_MISALIGNED;
     int sms = 0;
@@ -190,12 +225,45 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* 
     a.dbias_bf16 = dbias_dtype == VCD_BF16;
     a.shape = shape;
     a.plan = vcd::bwd_plan(S, C, policy, shape);
-    return cuda_status(vcd::launch_bwd(a, sms, stream));
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    a.xlist = exact ? reinterpret_cast<uint64_t*>(ws + xl.list_offset) : nullptr;
+    a.xcount = exact ? reinterpret_cast<uint32_t*>(ws + xl.count_offset) : nullptr;
+    a.xcap = exact ? xl.cap : 0;
+    return cuda_status(exact ? vcd::launch_bwd_exact(a, sms, stream) : vcd::launch_bwd(a, sms, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C, const void* weight,
+               int weight_dtype, const int32_t* cu_seqlens, int64_t num_docs, const void* bias,
+               int bias_dtype, int policy, void* dx, void* dweight, int dweight_dtype,
+               void* dbias, int dbias_dtype, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream) {
+    return bwd_call(x, dy, S, C, weight, weight_dtype, cu_seqlens, num_docs, bias, bias_dtype, policy,
+                    dx, dweight, dweight_dtype, dbias, dbias_dtype, workspace, workspace_bytes, stream,
+                    false);
+}
+
+int conv1d_bwd_exact(const void* x, const void* dy, int64_t S, int64_t C, const void* weight,
+                     int weight_dtype, const int32_t* cu_seqlens, int64_t num_docs, const void* bias,
+                     int bias_dtype, int policy, void* dx, void* dweight, int dweight_dtype,
+                     void* dbias, int dbias_dtype, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+    return bwd_call(x, dy, S, C, weight, weight_dtype, cu_seqlens, num_docs, bias, bias_dtype, policy,
+                    dx, dweight, dweight_dtype, dbias, dbias_dtype, workspace, workspace_bytes, stream,
+                    true);
 }
 
 int conv1d_wait_fault(int* flag) {
     if (!flag) return VCD_ERR_INVALID_ARG;
-    return cuda_status(vcd::read_wait_fault(flag));
+    int f = 0, b = 0;
+    const cudaError_t e = vcd::read_fwd_wait_fault(&f);
+    const cudaError_t e2 = vcd::read_wait_fault(&b);
+    if (e != cudaSuccess || e2 != cudaSuccess) return VCD_ERR_CUDA;
+    *flag = f | b;
+    return VCD_OK;
 }
 
 const char* conv1d_status_string(int status) {

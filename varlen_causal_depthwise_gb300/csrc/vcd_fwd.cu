@@ -18,6 +18,7 @@
 //
 // Memory-bound: 4 bytes of HBM traffic per element (read x, write y).
 #include <atomic>
+#include <type_traits>
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -42,35 +43,38 @@ constexpr int kFwdRowBytes = 2 * kFwdColCh;            // bytes of a token's row
 
 // Batch geometry of a forward shape (vcd_plan.h): tokens per batch and ring
 // stages.
+// kTma: the stages arrive by tensor-map copies (one per batch, issued by one
+// lane, onto an mbarrier) instead of per-lane cp.async -- faster where most
+// batches walk cu_seqlens and take the masked path (short documents: 110 ->
+// 104 us at 131072 x 1032), slower for streaming 4-token batches (65536 x
+// 6144: 254 -> 267 us; measured on GB300).
 template <int SHAPE> struct FwdGeom;
-template <> struct FwdGeom<kFwdStream> { static constexpr int kU = 4, kNs = 6; };
-template <> struct FwdGeom<kFwdShortDocs> { static constexpr int kU = 8, kNs = 3; };
+// kCtas: resident CTAs per SM the launch bounds promise (the exactness check
+// needs more registers).
+template <> struct FwdGeom<kFwdStream> {
+    static constexpr int kU = 4, kNs = 6, kCtas = kFwdCtasPerSm; static constexpr bool kTma = false;
+};
+template <> struct FwdGeom<kFwdShortDocs> {
+    static constexpr int kU = 8, kNs = 3, kCtas = kFwdCtasPerSm; static constexpr bool kTma = true;
+};
+template <> struct FwdGeom<kFwdExact> {
+    static constexpr int kU = 8, kNs = 3, kCtas = 2; static constexpr bool kTma = true;
+};
 template <int SHAPE> struct FwdShapeT : FwdGeom<SHAPE> {
     using G = FwdGeom<SHAPE>;
     static constexpr int kStageBytes = G::kU * kFwdRowBytes;
     static constexpr int kWarpBytes = G::kNs * kStageBytes;
-    static constexpr int kSmemBytes = kWarpsPerCta * kWarpBytes;
+    static constexpr int kRingBytes = kWarpsPerCta * kWarpBytes;
+    // the TMA ring's barriers, one 8-byte mbarrier per stage of each warp
+    static constexpr int kSmemBytes = kRingBytes + (G::kTma ? kWarpsPerCta * G::kNs * 8 : 0);
     static_assert(G::kU % 2 == 0 && G::kU <= 30 && G::kNs >= 2, "batch geometry");
 };
 
 __device__ __forceinline__ bool bit(uint32_t m, int i) { return (m >> i) & 1u; }
 
-// The taps and the bias with their dtypes chosen at run time (one uniform
-// branch per unit), for the instantiation that serves routes by run-time
-// dtype.
-__device__ __forceinline__ void load_taps_rt(const void* weight, const void* bias, bool w_bf16,
-                                             int bias_kind, int64_t c0, bool active,
-                                             float2 (&w)[4][2], float2 (&b)[2]) {
-    if (w_bf16) {
-        if (bias_kind == kBiasF32) load_taps<true, kBiasF32, 2>(weight, bias, c0, active, w, b);
-        else if (bias_kind == kBiasBF16) load_taps<true, kBiasBF16, 2>(weight, bias, c0, active, w, b);
-        else load_taps<true, kBiasNone, 2>(weight, bias, c0, active, w, b);
-    } else {
-        if (bias_kind == kBiasF32) load_taps<false, kBiasF32, 2>(weight, bias, c0, active, w, b);
-        else if (bias_kind == kBiasBF16) load_taps<false, kBiasBF16, 2>(weight, bias, c0, active, w, b);
-        else load_taps<false, kBiasNone, 2>(weight, bias, c0, active, w, b);
-    }
-}
+// Set when a forward kernel gave up waiting on a tile (mbar_wait_bounded);
+// never in normal operation. conv1d_wait_fault() reads it.
+__device__ int g_vcd_fwd_wait_fault = 0;
 
 // Routes by instantiation. The main loop is the same code for every route,
 // but the compiler schedules it differently per instantiation, and that moves
@@ -79,10 +83,31 @@ __device__ __forceinline__ void load_taps_rt(const void* weight, const void* bia
 // while BF16 weights with a bias run fastest through the one that takes the
 // dtypes at run time (65536 x 6144: 289 -> 260 us; 262144 x 8192: 1450 ->
 // 1342 us).
-constexpr int kRouteRuntime = -1;     // W_BF16 / BIAS template value: dtypes read at run time
+
+// A shape that stages by tensor-map copies gets the map with its arguments
+// (the streaming shape keeps the plain, smaller argument block).
+struct FwdTmaArgs : FwdArgs {
+    CUtensorMap tmap_x;       // x as [S rows, C channels], boxes of a batch x 128 channels
+};
+template <int SHAPE>
+using FwdParams = typename std::conditional<FwdGeom<SHAPE>::kTma, FwdTmaArgs, FwdArgs>::type;
+
+// The exactness check of conv1d_fwd_exact. An element's FP32 result y32 (an
+// FMA chain for pre, then SiLU from exp2 / reciprocal) is within 2^-10 |y| of
+// the exact y -- so that its BF16 rounding is within 3/4 of a BF16 ulp --
+// whenever mag (1 + |pre|) <= 4096 |pre|, mag = |b| + sum |w_k x_k| the
+// magnitude of the preactivation's terms: the chain errs by at most
+// 4 2^-24 mag, which SiLU carries into y with relative gain |1 + pre (1 - s)|
+// <= 1 + |pre|, and the SiLU evaluation adds at most (8 + |pre|) 2^-24
+// relative. The kernel tests the sufficient condition mag 2^-11 <= min(|pre|,
+// 1) with the magnitudes pre-scaled by 2^-11, and recomputes the elements
+// that fail it from their exactly summed preactivation.
+constexpr float kExactMagScale = 0x1p-11f;
 
 template <int SHAPE, bool W_BF16, int BIAS>
-__global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(kThreadsPerCta, FwdGeom<SHAPE>::kCtas)
+    fwd_kernel(const __grid_constant__ FwdParams<SHAPE> a) {
+    constexpr bool kTma = FwdGeom<SHAPE>::kTma;
     constexpr int kFwdU = FwdShapeT<SHAPE>::kU;                 // tokens per batch
     constexpr int kFwdNs = FwdShapeT<SHAPE>::kNs;               // ring stages
     constexpr int kFwdStageBytes = FwdShapeT<SHAPE>::kStageBytes;
@@ -101,6 +126,19 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
     const int32_t* __restrict__ cu = a.cu_seqlens;
     const int ncu = (int)(a.num_docs + 1);
     const int Ci = (int)C;                               // row stride, elements
+    // TMA: this warp's stage barriers (one arrival per phase: the producer
+    // lane's expect_tx), initialised once; phase parities in `phases`
+    const uint32_t bars = smem_u32(smem + FwdShapeT<SHAPE>::kRingBytes) + wid * kFwdNs * 8;
+    uint32_t phases = 0;
+    bool fault = false;
+    if (kTma) {
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < kFwdNs; ++s) mbar_init(bars + 8 * s, 1);
+            mbar_init_fence();
+        }
+        __syncwarp();
+    }
 
     for (int64_t u = warp0; u < units; u += nwarps) {
         const int64_t col = u % ncols, row = u / ncols;
@@ -125,37 +163,51 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
         for (int k = 0; k < 3; ++k) xc[k][0] = xc[k][1] = zero2();
 
         RowStream<1, kFwdRowBytes, int64_t> rs;
-        {
+        if (!kTma) {
             const __nv_bfloat16* const bases[1] = {x};
             const int64_t lows[1] = {q0 > 0 ? q0 : 0};
             rs.init(bases, C, col, q0, lows, t_end, lane);
         }
+        auto issue = [&](int i, int slot) {
+            if constexpr (kTma) {
+                // the tile of tokens q0 + i U .. + U - 1 x the column's 128
+                // channels (rows outside [0, S) and channels past C arrive as
+                // zeros; rows past the unit are never read)
+                if (i < nb && lane == 0) {
+                    const uint32_t bar = bars + 8 * slot;
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(bar, kFwdStageBytes);
+                    tma_load_2d(ring_s + slot * kFwdStageBytes, &a.tmap_x, (int)(col * kFwdColCh),
+                                (int)q0 + i * kFwdU, bar);
+                }
+            } else {
+                if (i < nb) {
+                    const uint32_t d[1] = {ring_s + slot * kFwdStageBytes};
+                    rs.stage<kFwdU>(d, i * kFwdU, x);
+                }
+                cp_async_commit();
+            }
+        };
         __nv_bfloat16* yp = y + q0 * C + c0;                   // y row of relative token 0
         const int64_t ystep = C;
 
         __syncwarp();                    // the previous unit's reads of the ring are done
 #pragma unroll
-        for (int s = 0; s < kFwdNs - 1; ++s) {
-            if (s < nb) {
-                const uint32_t d[1] = {ring_s + s * kFwdStageBytes};
-                rs.stage<kFwdU>(d, s * kFwdU, x);
-            }
-            cp_async_commit();
-        }
+        for (int s = 0; s < kFwdNs - 1; ++s) issue(s, s);
 
         int slot = 0;                    // ring stage of batch i
         for (int i = 0; i < nb; ++i) {
-            cp_async_wait<kFwdNs - 2>();
-            __syncwarp();
-            {
-                const int nx = i + kFwdNs - 1;
-                const int nslot = slot == 0 ? kFwdNs - 1 : slot - 1;   // (i + Ns - 1) % Ns
-                if (nx < nb) {
-                    const uint32_t d[1] = {ring_s + nslot * kFwdStageBytes};
-                    rs.stage<kFwdU>(d, nx * kFwdU, x);
+            if constexpr (kTma) {
+                if (!mbar_wait_bounded(bars + 8 * slot, (phases >> slot) & 1u)) {
+                    fault = true;
+                    break;
                 }
-                cp_async_commit();
+                phases ^= 1u << slot;
+            } else {
+                cp_async_wait<kFwdNs - 2>();
             }
+            __syncwarp();
+            issue(i + kFwdNs - 1, slot == 0 ? kFwdNs - 1 : slot - 1);   // (i + Ns - 1) % Ns
             const int r0 = i * kFwdU;                    // relative index of the batch
             const int64_t q = q0 + r0;
             const uint32_t nw = doc.starts(cu, ncu, (int)q, kFwdU, lane);
@@ -164,7 +216,65 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
             const unsigned char* st = ring + slot * kFwdStageBytes + lane * (2 * kFwdVec);
             __nv_bfloat16* yq = yp + (int64_t)r0 * ystep;
 
-            if (M == 0 && r0 >= 3 && r0 + kFwdU <= n_rel) {      // every token stored
+            if constexpr (SHAPE == kFwdExact) {
+                // every batch through one predicated path, each element checked
+#pragma unroll
+                for (int j = 0; j < kFwdU; ++j) {
+                    const int r = r0 + j;
+                    const uint2 xv = lds64(st + j * kFwdRowBytes);
+                    const float2 xf[2] = {bf16x2_to_float2(xv.x), bf16x2_to_float2(xv.y)};
+                    const bool m1 = !bit(M, j + 2);
+                    const bool m2 = m1 && !bit(M, j + 1);
+                    const bool m3 = m2 && !bit(M, j);
+                    float2 yv[2];
+                    uint32_t doubt = 0;                  // bit 2p + h: channel 2p + h needs recomputing
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        float2 pre = b[p];
+                        float2 mag = make_float2(fabsf(b[p].x) * kExactMagScale, fabsf(b[p].y) * kExactMagScale);
+                        const float2 xs[4] = {xc[0][p], xc[1][p], xc[2][p], xf[p]};
+                        const bool on[4] = {m3, m2, m1, true};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (!on[k]) continue;
+                            pre = fma2<false>(w[k][p], xs[k], pre);
+                            mag.x = __fmaf_rn(fabsf(w[k][p].x) * kExactMagScale, fabsf(xs[k].x), mag.x);
+                            mag.y = __fmaf_rn(fabsf(w[k][p].y) * kExactMagScale, fabsf(xs[k].y), mag.y);
+                        }
+                        yv[p] = silu2<false>(pre);
+                        if (mag.x > fminf(fabsf(pre.x), 1.0f)) doubt |= 1u << (2 * p);
+                        if (mag.y > fminf(fabsf(pre.y), 1.0f)) doubt |= 2u << (2 * p);
+                    }
+                    if (__any_sync(kFull, doubt != 0)) {
+                        // rare: those elements from their exactly summed
+                        // preactivation (one FP32 rounding), then SiLU
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (!((doubt >> e) & 1u)) continue;
+                            const int p = e >> 1;
+                            const bool hi = e & 1;
+                            const float bb = hi ? b[p].y : b[p].x;
+                            const float wk[4] = {hi ? w[0][p].y : w[0][p].x, hi ? w[1][p].y : w[1][p].x,
+                                                 hi ? w[2][p].y : w[2][p].x, hi ? w[3][p].y : w[3][p].x};
+                            const float xk[4] = {hi ? xc[0][p].y : xc[0][p].x, hi ? xc[1][p].y : xc[1][p].x,
+                                                 hi ? xc[2][p].y : xc[2][p].x, hi ? xf[p].y : xf[p].x};
+                            const bool on[4] = {m3, m2, m1, true};
+                            const float pe = (float)exact_preactivation(bb, wk, xk, on);
+                            const float ye = silu2<false>(make_float2(pe, pe)).x;
+                            if (hi) yv[p].y = ye; else yv[p].x = ye;
+                        }
+                    }
+                    uint32_t o[2];
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        o[p] = float2_to_bf16x2(yv[p]);
+                        xc[0][p] = xc[1][p];
+                        xc[1][p] = xc[2][p];
+                        xc[2][p] = xf[p];
+                    }
+                    if (active && r >= 3 && r < n_rel) st_stream(yq + j * Ci, make_uint2(o[0], o[1]));
+                }
+            } else if (M == 0 && r0 >= 3 && r0 + kFwdU <= n_rel) {      // every token stored
 #pragma unroll
                 for (int j = 0; j < kFwdU; ++j) {
                     const uint2 xv = lds64(st + j * kFwdRowBytes);
@@ -239,6 +349,14 @@ __global__ void __launch_bounds__(kThreadsPerCta, kFwdCtasPerSm) fwd_kernel(cons
             }
             slot = slot + 1 == kFwdNs ? 0 : slot + 1;
         }
+        if (kTma && fault) break;
+    }
+    if (kTma && fault) {
+        // a tile never arrived: flag it and give the stages still in flight a
+        // bounded wait before the warp leaves
+        if (lane == 0) atomicExch(&g_vcd_fwd_wait_fault, 1);
+#pragma unroll
+        for (int s = 0; s < kFwdNs; ++s) mbar_wait_bounded(bars + 8 * s, (phases >> s) & 1u);
     }
 }
 
@@ -265,7 +383,14 @@ int prepare_t() {
 }
 
 template <int SHAPE, bool W_BF16, int BIAS>
-cudaError_t launch_fwd_t(const FwdArgs& a, int sm_count, cudaStream_t stream) {
+cudaError_t launch_fwd_t(const FwdArgs& args, int sm_count, cudaStream_t stream) {
+    FwdParams<SHAPE> a;
+    static_cast<FwdArgs&>(a) = args;
+    if constexpr (FwdGeom<SHAPE>::kTma) {
+        const cudaError_t e = encode_bf16_rows(&a.tmap_x, a.x, a.plan.S, a.plan.C, kFwdColCh,
+                                               FwdGeom<SHAPE>::kU);
+        if (e != cudaSuccess) return e;
+    }
     const int occ = prepare_t<SHAPE, W_BF16, BIAS>();
     if (occ <= 0) return cudaErrorInvalidConfiguration;
     const int64_t ctas_needed = (a.plan.units + kWarpsPerCta - 1) / kWarpsPerCta;
@@ -280,6 +405,17 @@ cudaError_t launch_fwd_t(const FwdArgs& a, int sm_count, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t read_fwd_wait_fault(int* flag) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(flag, g_vcd_fwd_wait_fault, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_vcd_fwd_wait_fault, &zero, sizeof(int));
+    return e;
+}
+
+cudaError_t launch_fwd_exact(const FwdArgs& a, int sm_count, cudaStream_t stream) {
+    return launch_fwd_t<kFwdExact, false, kRouteRuntime>(a, sm_count, stream);
+}
 
 cudaError_t launch_fwd(const FwdArgs& a, int sm_count, cudaStream_t stream) {
     typedef cudaError_t (*L)(const FwdArgs&, int, cudaStream_t);

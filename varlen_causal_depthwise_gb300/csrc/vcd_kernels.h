@@ -43,6 +43,13 @@ struct BwdArgs {
     int dbias_bf16;
     int shape;                // BwdShape
     BwdPlan plan;             // bwd_plan(S, C, policy, shape)
+    // The exactness-guarded route (conv1d_bwd_exact): per chunk a list of
+    // xcap dx elements (token << 32 | channel) whose FP32 value it could not
+    // certify, and their count (may exceed xcap: then the whole chunk is
+    // recomputed); null otherwise.
+    uint64_t* xlist;
+    uint32_t* xcount;
+    int64_t xcap;
     // 2D tensor maps of x and dy ([S rows, C channels] BF16, boxes of the
     // shape's batch of tokens x 128 channels), filled by launch_bwd.
     CUtensorMap tmap_x;
@@ -50,6 +57,14 @@ struct BwdArgs {
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, int sm_count, cudaStream_t stream);
+// The exactness-guarded forward (conv1d_fwd_exact).
+cudaError_t launch_fwd_exact(const FwdArgs& a, int sm_count, cudaStream_t stream);
+// The forward's wait-fault flag, read and cleared; synchronous.
+cudaError_t read_fwd_wait_fault(int* flag);
+// A [S, C] BF16 tensor as a 2D tensor map (channels innermost) with boxes of
+// `rows` tokens x `cols` channels; elements outside the tensor read as zero.
+cudaError_t encode_bf16_rows(CUtensorMap* m, const void* base, int64_t S, int64_t C, int cols,
+                             int rows);
 // conv1d_bwd's argument checks, all but the workspace's (vcd_capi.cu); a
 // vcd_status code.
 int check_bwd_args(const void* x, const void* dy, int64_t S, int64_t C, const void* weight,
@@ -58,6 +73,9 @@ int check_bwd_args(const void* x, const void* dy, int64_t S, int64_t C, const vo
                    int dweight_dtype, const void* dbias, int dbias_dtype);
 // Main kernel, then the reduce kernel launched programmatically dependent on it.
 cudaError_t launch_bwd(const BwdArgs& a, int sm_count, cudaStream_t stream);
+// The exactness-guarded backward (conv1d_bwd_exact): the main kernel with
+// its checks, the reduce, then the recomputation of the listed dx elements.
+cudaError_t launch_bwd_exact(const BwdArgs& a, int sm_count, cudaStream_t stream);
 // The backward's wait-fault flag (set, never in normal operation, when a
 // kernel gave up waiting on a tile), read and cleared; synchronous.
 cudaError_t read_wait_fault(int* flag);

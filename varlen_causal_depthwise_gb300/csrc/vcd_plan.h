@@ -42,7 +42,10 @@ constexpr int64_t kFwdTargetUnits = kGb300Sms * kFwdCtasPerSm * kWarpsPerCta;
 // batches, so each batch walks cu_seqlens and takes the masked path) take
 // 8-token batches in a 3-stage ring, which halves those per-batch costs. The
 // choice changes no result, only the time.
-enum FwdShape { kFwdStream = 0, kFwdShortDocs = 1 };
+// kFwdExact is the exactness-guarded route (conv1d_fwd_exact): 8-token
+// batches on every workload, each element checked and the doubtful ones
+// recomputed (vcd_fwd.cu).
+enum FwdShape { kFwdStream = 0, kFwdShortDocs = 1, kFwdExact = 2 };
 
 // Backward launch shapes: one CTA per SM either way; they trade registers for
 // warps.
@@ -176,6 +179,38 @@ inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy) {
 inline uint64_t bwd_call_workspace_bytes(int64_t S, int64_t C, int64_t num_docs, int policy,
                                          bool has_bias) {
     return bwd_workspace_bytes_for(S, C, policy, bwd_shape(S, num_docs, policy, has_bias));
+}
+
+// The exactness-guarded backward (conv1d_bwd_exact) runs the chunked shape
+// for both policies and adds, per chunk, a list of dx elements to recompute:
+// room for one in 256 of the chunk's elements (at least 64), 8 bytes each,
+// then one 4-byte count per chunk. The layout after the partial rows, each
+// part starting on a 16-byte boundary.
+inline int64_t exact_list_cap(const BwdPlan& p) {
+    const int64_t elems = p.L * p.per * p.col_channels;
+    const int64_t cap = elems / 256;
+    return cap > 64 ? cap : 64;
+}
+inline uint64_t round16(uint64_t n) { return (n + 15) & ~(uint64_t)15; }
+struct ExactLayout {
+    uint64_t partial_bytes, list_offset, count_offset, total;
+    int64_t cap;
+};
+inline ExactLayout exact_layout(int64_t S, int64_t C, int policy) {
+    ExactLayout e = {0, 0, 0, 0, 0};
+    if (S <= 0) return e;
+    const BwdPlan p = bwd_plan(S, C, policy, kBwdChunked);
+    const uint64_t lists = (uint64_t)p.chunks * p.ncols;
+    e.cap = exact_list_cap(p);
+    e.partial_bytes = round16(bwd_workspace_bytes_for(S, C, policy, kBwdChunked));
+    e.list_offset = e.partial_bytes;
+    e.count_offset = round16(e.list_offset + lists * (uint64_t)e.cap * 8);
+    e.total = round16(e.count_offset + lists * 4);
+    return e;
+}
+inline uint64_t bwd_exact_workspace_bytes(int64_t S, int64_t C) {
+    const uint64_t a = exact_layout(S, C, 0).total, b = exact_layout(S, C, 1).total;
+    return a > b ? a : b;
 }
 
 // The most any route needs.
