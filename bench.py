@@ -292,12 +292,19 @@ def run_ours(args):
     dB = None if w.bias is None else torch.empty(C, dtype=w.bias.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    if args.exact:
+        wsp = torch.empty(vcd.conv1d_bwd_exact_workspace_size(S, C), dtype=torch.uint8, device=dev)
+
     def fwd():
-        vcd.conv1d_fwd(w.x, w.weight, w.cu_seqlens, w.bias, y=y, stream=stream)
+        if args.exact:
+            vcd.conv1d_fwd_exact(w.x, w.weight, w.cu_seqlens, w.bias, y=y, stream=stream)
+        else:
+            vcd.conv1d_fwd(w.x, w.weight, w.cu_seqlens, w.bias, y=y, stream=stream)
 
     def bwd():
-        vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, policy, dx=dx, dweight=dW,
-                       dbias=dB, workspace=wsp, stream=stream)
+        entry = vcd.conv1d_bwd_exact if args.exact else vcd.conv1d_bwd
+        entry(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, policy, dx=dx, dweight=dW, dbias=dB,
+              workspace=wsp, stream=stream)
 
     for _ in range(args.warmup):
         fwd()
@@ -554,7 +561,8 @@ def finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws
         "config": {"workload": f"{args.config}: S={S}, C={C}, {w.num_docs} docs, "
                                f"weight {str(w.weight.dtype)[6:]}, "
                                f"bias {'none' if w.bias is None else str(w.bias.dtype)[6:]}, "
-                               f"SiLU' policy {policy}, BF16 x/dy/y/dx",
+                               f"SiLU' policy {policy}, BF16 x/dy/y/dx"
+                               + (", exactness-guarded routes" if args.exact else ""),
                    "S": S, "C": C, "num_docs": w.num_docs, "policy": policy,
                    "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (no flush needed)"},
@@ -576,7 +584,7 @@ def finish(args, w, S, C, policy, nws, K, total_ms, fwd_ms, bwd_ms, clk, e2e, ws
             "value": round(ws * step_b / (e2e[0] * 1e-3) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(e2e[0], 3), "h2d_bytes_per_step": e2e[1],
             "d2h_bytes_per_step": e2e[2]},
-        "gpu_launches": 3 * K,
+        "gpu_launches": (4 if args.exact else 3) * K,
         **({"routes": extra["routes"]} if "routes" in extra else {}),
         "clocks": clocks,
         "kernel_sha": sha,
@@ -722,6 +730,8 @@ def main():
                          "when --steps is large, so the arm's K steps take about a minute)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--exact", action="store_true",
+                    help="time the exactness-guarded routes (conv1d_fwd_exact, conv1d_bwd_exact)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the per-workload / per-policy timings (routes)")
     ap.add_argument("--S", type=int, default=None,

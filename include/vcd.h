@@ -169,7 +169,7 @@ int conv1d_bwd(const void* x, const void* dy, int64_t S, int64_t C,
 
 /* Bytes of workspace conv1d_bwd_exact needs for (S, C), either policy: the
  * partial rows of its launch shape, then per chunk of work a list of the dx
- * elements to recompute (room for one in 256 elements) and its count. Errors
+ * elements to recompute (room for one in 64 elements) and its count. Errors
  * as conv1d_bwd_workspace_size. */
 int conv1d_bwd_exact_workspace_size(int64_t S, int64_t C, size_t* bytes);
 
@@ -183,8 +183,9 @@ int conv1d_bwd_exact_workspace_size(int64_t S, int64_t C, size_t* bytes);
  * cancels, or, under "bf16", where the FP32 preactivation and the exact one
  * round to different BF16 values. This route takes the preactivations near a
  * BF16 rounding midpoint from their exact sum, evaluates SiLU' to about
- * 2^-22, bounds each dx's FP32 error, and recomputes in FP64 the few (a few
- * in 10^4) that the bound cannot certify, in a third launch after the reduce.
+ * 2^-22, bounds each dx's FP32 error, and recomputes the few (a few in 10^3)
+ * that the bound cannot certify in double-float arithmetic (about 2^-44), in
+ * a third launch after the reduce.
  * dweight and dbias are formed as in conv1d_bwd (same tolerances); under
  * "bf16" they use the exactly rounded preactivations. Slower than conv1d_bwd. */
 int conv1d_bwd_exact(const void* x, const void* dy, int64_t S, int64_t C,

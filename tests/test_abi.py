@@ -232,7 +232,7 @@ def test_noalloc_limits_stated_in_the_header(lib, S, C, policy, fits):
 
 def test_exact_workspace_query(lib):
     """The exactness-guarded backward's workspace: its launch shape's partial
-    rows, then per chunk a list with room for one in 256 of the chunk's
+    rows, then per chunk a list with room for one in 64 of the chunk's
     elements (at least 64 entries of 8 bytes) and a 4-byte count, each part on
     a 16-byte boundary; 0 for S == 0; errors like the other queries."""
     assert vcd.conv1d_bwd_exact_workspace_size(0, 256) == 0
@@ -241,10 +241,10 @@ def test_exact_workspace_query(lib):
         assert n % 16 == 0
         assert n > max(vcd.conv1d_bwd_call_workspace_size(S, C, 1, p, True) for p in ("bf16", "fp32"))
     # 65536 x 6144 in the chunked shape (1824 target warps): "bf16" 38 chunks
-    # of 1725 tokens per column, lists of 1725 * 128 / 256 = 862 entries;
-    # "fp32" 37 chunks of 7 units of 256 tokens, lists of 896; the larger
-    bf = 48 * 38 * (2560 + 862 * 8 + 4)
-    fp = 48 * 37 * (2560 + 896 * 8 + 4)
+    # of 1725 tokens per column, lists of 1725 * 128 / 64 = 3450 entries;
+    # "fp32" 37 chunks of 7 units of 256 tokens, lists of 3584; the larger
+    bf = 48 * 38 * (2560 + 3450 * 8 + 4)
+    fp = 48 * 37 * (2560 + 3584 * 8 + 4)
     assert abs(vcd.conv1d_bwd_exact_workspace_size(65536, 6144) - max(bf, fp)) <= 32
     with pytest.raises(vcd.VcdError):
         vcd.conv1d_bwd_exact_workspace_size(8, 12)

@@ -37,6 +37,7 @@
 #include <stdint.h>
 
 #include "vcd_device.cuh"
+#include "vcd_dfloat.cuh"
 #include "vcd_kernels.h"
 #include "vcd_plan.h"
 
@@ -122,6 +123,13 @@ __device__ __forceinline__ float2 grad_at(float2 pre) {
 // kRouteRuntime (dtypes read at run time).
 constexpr float kU24 = 0x1p-24f;                  // FP32 unit roundoff
 constexpr float kExactScale = 0x1p-11f;           // magnitudes are kept scaled by this
+// Absolute error bound of silu_grad_accurate_nc (about 12 2^-24 for every
+// p), with margin.
+constexpr float kExactGradErr = 0x1p-24f * 24.0f;
+// A dx whose FP32 value v is within 2^-9 |v| of the exact value rounds to
+// BF16 within one ulp of it (|v| < 2^8 ulp(v), so the rounding's half ulp
+// plus 2^-9 |v| stays below one ulp); larger error bounds are recomputed.
+constexpr float kExactAccept = 0x1p-9f;
 
 template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG, bool EXACT = false>
 __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
@@ -314,13 +322,15 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
         //    (4 2^-24 mag, mag = the magnitude of its terms) of a BF16
         //    rounding midpoint is summed exactly before it is rounded, so p
         //    is the rounding of the exact preactivation;
-        //  - SiLU' by the accurate evaluation for both policies;
-        //  - a bound on each dpre's error (e: SiLU' evaluation (16 + 16|p|)
-        //    2^-24 times |dy|, the product's rounding, and under "fp32" the
+        //  - SiLU' by the accurate, cancellation-free evaluation for both
+        //    policies;
+        //  - a bound on each dpre's error (e: SiLU' evaluation kExactGradErr
+        //    times |dy|, the product's rounding, and under "fp32" the
         //    preactivation's error times max|silu''| = 1/2) and on dx's:
-        //    sum |w| e + 5 2^-24 sum |w dpre|. A dx whose bound exceeds 2^-10
-        //    of its value goes to the chunk's list (its BF16 rounding might
-        //    miss the 1-ulp bound) and is recomputed in FP64 afterwards.
+        //    sum |w| e + 5 2^-24 sum |w dpre|. A dx whose bound exceeds
+        //    kExactAccept of its value goes to the chunk's list (its BF16
+        //    rounding might miss the 1-ulp bound) and is recomputed afterwards
+        //    in double-float arithmetic.
         auto exact_token = [&](int r, const uint32_t (&xv)[kNP], const uint32_t (&gv)[kNP], bool m1,
                                bool m2, bool m3, bool k1, bool k2, bool k3, bool has_d, bool acc,
                                bool emit, uint32_t (&o)[kNP]) {
@@ -376,12 +386,11 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
             for (int p = 0; p < kNP; ++p) {
                 float2 d = zero2(), ed = zero2();
                 if (has_d) {
-                    const float2 g = silu_grad2_accurate(pt[p]);
+                    const float2 g = make_float2(silu_grad_accurate_nc(pt[p].x),
+                                                 silu_grad_accurate_nc(pt[p].y));
                     d = mul2<false>(gf[p], g);
-                    const float2 eg = make_float2(kU24 * (16.0f + 16.0f * fabsf(pt[p].x)),
-                                                  kU24 * (16.0f + 16.0f * fabsf(pt[p].y)));
-                    ed.x = __fmaf_rn(fabsf(gf[p].x), eg.x, kU24 * fabsf(d.x));
-                    ed.y = __fmaf_rn(fabsf(gf[p].y), eg.y, kU24 * fabsf(d.y));
+                    ed.x = __fmaf_rn(fabsf(gf[p].x), kExactGradErr, kU24 * fabsf(d.x));
+                    ed.y = __fmaf_rn(fabsf(gf[p].y), kExactGradErr, kU24 * fabsf(d.y));
                     if (POLICY == kPolicyFP32) {          // |silu''| <= 1/2 times 4 2^-24 mag
                         ed.x = __fmaf_rn(fabsf(gf[p].x), mag[p].x * (0.5f * kExactScale), ed.x);
                         ed.y = __fmaf_rn(fabsf(gf[p].y), mag[p].y * (0.5f * kExactScale), ed.y);
@@ -413,8 +422,8 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
                     ex = __fmaf_rn(aw.x, __fmaf_rn(5.0f * kU24, fabsf(ds[i].x), es[i].x), ex);
                     ey = __fmaf_rn(aw.y, __fmaf_rn(5.0f * kU24, fabsf(ds[i].y), es[i].y), ey);
                 }
-                if (emit && ex > 0x1p-10f * fabsf(g.x)) doubt |= 1u << (2 * p);
-                if (emit && ey > 0x1p-10f * fabsf(g.y)) doubt |= 2u << (2 * p);
+                if (emit && ex > kExactAccept * fabsf(g.x)) doubt |= 1u << (2 * p);
+                if (emit && ey > kExactAccept * fabsf(g.y)) doubt |= 2u << (2 * p);
                 xc[0][p] = xc[1][p];
                 xc[1][p] = xc[2][p];
                 xc[2][p] = xf[p];
@@ -761,22 +770,15 @@ __device__ int64_t doc_start_of(const int32_t* __restrict__ cu, int ncu, int64_t
     return s < 0 ? 0 : s > t ? t : s;
 }
 
-__device__ double param_at(const void* base, bool bf16, int64_t i) {
-    if (bf16) return (double)__bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
-    return (double)reinterpret_cast<const float*>(base)[i];
+__device__ float param_at(const void* base, bool bf16, int64_t i) {
+    if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
+    return reinterpret_cast<const float*>(base)[i];
 }
 
-// sigmoid(p) for either sign without overflow.
-__device__ double sigmoid64(double p) {
-    if (p >= 0.0) return 1.0 / (1.0 + exp(-p));
-    const double e = exp(p);
-    return e / (1.0 + e);
-}
-
-// dx[t, c] of the policy in FP64 from the inputs: each preactivation summed
-// exactly (the products of FP32 or BF16 weights and BF16 inputs are exact in
-// FP64; compensated sums), SiLU' at the policy's point, and the four-term sum,
-// rounded once to BF16.
+// dx[t, c] of the policy from the inputs, to about 2^-44 before its one
+// rounding to BF16: each preactivation summed exactly (exact_preactivation),
+// SiLU' at the policy's point in double-float arithmetic, the products with
+// dy and the weights and the four-term sum in double-float.
 __device__ __nv_bfloat16 dx_exact(const BwdArgs& a, int64_t t, int64_t c) {
     const int64_t S = a.plan.S, C = a.plan.C;
     const int32_t* cu = a.cu_seqlens;
@@ -784,33 +786,35 @@ __device__ __nv_bfloat16 dx_exact(const BwdArgs& a, int64_t t, int64_t c) {
     const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
     const __nv_bfloat16* dy = static_cast<const __nv_bfloat16*>(a.dy);
     const bool wb = a.weight_bf16 != 0;
-    double wk[4];
+    float wk[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) wk[k] = param_at(a.weight, wb, c * 4 + k);
-    const double bias = a.bias_kind == kBiasNone ? 0.0 : param_at(a.bias, a.bias_kind == kBiasBF16, c);
+    const float bias = a.bias_kind == kBiasNone ? 0.0f : param_at(a.bias, a.bias_kind == kBiasBF16, c);
     const int64_t s0 = doc_start_of(cu, ncu, t);
-    double sum = 0.0, comp = 0.0;
+    dfloat acc = df_of(0.0f);
     for (int k = 0; k < 4; ++k) {
         const int64_t j = t + 3 - k;                         // the token whose pre used x[t] via tap k
         if (j >= S || doc_start_of(cu, ncu, j) != s0) continue;
-        double pre = bias, pc = 0.0;
+        float xs[4];
+        bool on[4];
+#pragma unroll
         for (int m = 0; m < 4; ++m) {
             const int64_t i = j - 3 + m;
-            if (i < s0) continue;
-            const double v = wk[m] * (double)__bfloat162float(x[i * C + c]);
-            const double u = pre + v;
-            pc += fabs(pre) >= fabs(v) ? (pre - u) + v : (v - u) + pre;
-            pre = u;
+            on[m] = i >= s0;
+            xs[m] = on[m] ? __bfloat162float(x[i * C + c]) : 0.0f;
         }
-        pre += pc;
-        const double p = a.policy == kPolicyBF16 ? (double)__bfloat162float(__double2bfloat16(pre)) : pre;
-        const double g = sigmoid64(p) * (1.0 + p * sigmoid64(-p));
-        const double term = wk[k] * ((double)__bfloat162float(dy[j * C + c]) * g);
-        const double u = sum + term;
-        comp += fabs(sum) >= fabs(term) ? (sum - u) + term : (term - u) + sum;
-        sum = u;
+        const double pre = exact_preactivation(bias, wk, xs, on);
+        dfloat p;
+        if (a.policy == kPolicyBF16) {
+            p = df_of(__bfloat162float(__double2bfloat16(pre)));
+        } else {
+            p.hi = (float)pre;
+            p.lo = (float)(pre - (double)p.hi);
+        }
+        const dfloat dpre = df_mul_f(df_silu_grad(p), __bfloat162float(dy[j * C + c]));
+        acc = df_add(acc, df_mul_f(dpre, wk[k]));
     }
-    return __double2bfloat16(sum + comp);
+    return pair_to_bf16(acc.hi, acc.lo);
 }
 
 // Recomputes the dx elements the guarded main kernel listed, one list (one

@@ -183,12 +183,12 @@ inline uint64_t bwd_call_workspace_bytes(int64_t S, int64_t C, int64_t num_docs,
 
 // The exactness-guarded backward (conv1d_bwd_exact) runs the chunked shape
 // for both policies and adds, per chunk, a list of dx elements to recompute:
-// room for one in 256 of the chunk's elements (at least 64), 8 bytes each,
-// then one 4-byte count per chunk. The layout after the partial rows, each
-// part starting on a 16-byte boundary.
+// room for one in 64 of the chunk's elements (at least 64; a few in 10^3 are
+// listed on normal inputs), 8 bytes each, then one 4-byte count per chunk.
+// The layout after the partial rows, each part starting on a 16-byte boundary.
 inline int64_t exact_list_cap(const BwdPlan& p) {
     const int64_t elems = p.L * p.per * p.col_channels;
-    const int64_t cap = elems / 256;
+    const int64_t cap = elems / 64;
     return cap > 64 ? cap : 64;
 }
 inline uint64_t round16(uint64_t n) { return (n + 15) & ~(uint64_t)15; }
