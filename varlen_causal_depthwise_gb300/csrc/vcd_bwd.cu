@@ -480,7 +480,9 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
             // tokens back (a unit boundary, if any, is at position 3)
             const bool interior = r0 >= 6 && r0 + kBwdU <= r_end;
             if constexpr (EXACT) {
-#pragma unroll
+                // not unrolled: the guarded body is long, and kBwdU copies of
+                // it overflow the instruction cache (measured)
+#pragma unroll 1
                 for (int j = 0; j < kBwdU; ++j) {
                     const int r = r0 + j;
                     if (j == 3) unit_boundary(r);

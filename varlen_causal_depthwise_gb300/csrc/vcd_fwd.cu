@@ -217,8 +217,9 @@ __global__ void __launch_bounds__(kThreadsPerCta, FwdGeom<SHAPE>::kCtas)
             __nv_bfloat16* yq = yp + (int64_t)r0 * ystep;
 
             if constexpr (SHAPE == kFwdExact) {
-                // every batch through one predicated path, each element checked
-#pragma unroll
+                // every batch through one predicated path, each element
+                // checked; not unrolled (the instruction cache, measured)
+#pragma unroll 1
                 for (int j = 0; j < kFwdU; ++j) {
                     const int r = r0 + j;
                     const uint2 xv = lds64(st + j * kFwdRowBytes);
