@@ -10,27 +10,32 @@
 //   dw[k]    sum_t dpre[t] x[t - 3 + k]  (zero history)
 //   db       sum_t dpre[t]
 //
-// Main kernel: one warp per work unit (32 * kBwdVec channels x L tokens,
-// vcd_plan.h), walking its tokens forward once, in one of two launch shapes
-// picked per call (one CTA of 12 warps per SM with up to 168 registers a
-// thread, or 16 warps with 128; BwdGeom below). x and dy stream through a
-// per-warp shared-memory ring (cp.async, kBwdNs - 1 batches of kBwdU tokens
-// ahead). Registers hold the x of the three previous tokens and their dpre,
-// so each token gives pre, dpre, its dweight / dbias products, and dx of the
-// token three back in gather form:
+// Main kernel: one warp per chunk of work units (32 * kBwdVec channels x L
+// tokens each, vcd_plan.h), walking its tokens forward once, in one of three
+// launch shapes picked per call (12 warps per SM with up to 168 registers a
+// thread, 16 warps with 128, or 12 warps with shared memory for the "fp32"
+// policy's compensated chunk sums; BwdGeom below). x and dy stream through a
+// per-warp shared-memory ring of kBwdNs stages: one lane issues two 2D
+// tensor-map copies (TMA) per batch of kBwdU tokens onto the stage's
+// mbarrier, kBwdNs - 1 batches ahead. Registers hold the x of the three
+// previous tokens and their dpre, so each token gives pre, dpre, its dweight /
+// dbias products, and dx of the token three back in gather form:
 //   dx[t-3] = w3 dpre[t-3] + w2 dpre[t-2] + w1 dpre[t-1] + w0 dpre[t].
 // A batch without a document start in positions q-2 .. q+U-1 (one bit mask
 // per batch from cu_seqlens) takes a mask-free path; otherwise each term is
 // predicated on "no document start in between". The unit reads x over
 // [begin-3, end+3) and dy over [begin, end+3), writes dx over [begin, end),
 // and keeps dweight / dbias in registers; at its end each lane writes its
-// channels' five FP32 sums into the unit's partial row. HBM traffic: 6 bytes
-// per element.
+// channels' five FP32 sums into the chunk's partial row (or folds them into
+// the chunk's compensated sums). HBM traffic: 6 bytes per element.
 //
 // Reduce kernel: launched with programmatic stream serialization, it waits on
 // griddepcontrol for the main kernel and sums the partial rows of each channel
-// in a fixed order (FP32, or FP64 under the "fp32" policy), so the gradients
-// are bitwise reproducible for a given (S, C) and route.
+// in a fixed order (FP32, or compensated FP32 pairs under the "fp32" policy),
+// so the gradients are bitwise reproducible for a given (S, C) and route.
+//
+// The exactness-guarded route (conv1d_bwd_exact) runs the main kernel with
+// EXACT = true and a third kernel that recomputes the listed dx elements.
 #include <atomic>
 
 #include <cuda_runtime.h>
@@ -46,10 +51,6 @@ namespace {
 
 #ifndef VCD_BWD_PACKED
 #define VCD_BWD_PACKED 0
-#endif
-// x and dy stages by tensor-map copies (1) or by per-lane cp.async (0).
-#ifndef VCD_BWD_TMA
-#define VCD_BWD_TMA 1
 #endif
 #ifndef VCD_BWD_PACKED_ACC
 #define VCD_BWD_PACKED_ACC 0
@@ -83,7 +84,7 @@ template <int SHAPE> struct BwdShapeT : BwdGeom<SHAPE> {
     // the TMA ring's barriers: one 8-byte mbarrier per stage of each warp
     static constexpr int kBarBytes = G::kWarps * G::kNs * 8;
     template <bool SEG> static constexpr int smem_bytes() {
-        return kSmemBytes + (SEG ? kAccBytes : 0) + (VCD_BWD_TMA ? kBarBytes : 0);
+        return kSmemBytes + (SEG ? kAccBytes : 0) + kBarBytes;
     }
 };
 // Units of several per chunk are the "fp32" policy's, kFp32TokensPerUnit
@@ -107,9 +108,9 @@ constexpr int kPolicyFP32 = 1;
 
 __device__ __forceinline__ bool bit(uint32_t m, int i) { return (m >> i) & 1u; }
 
-template <int POLICY>
+template <int POLICY, bool PK = kPK>
 __device__ __forceinline__ float2 grad_at(float2 pre) {
-    if (POLICY == kPolicyBF16) return silu_grad2<kPK>(round_bf16x2(pre));
+    if (POLICY == kPolicyBF16) return silu_grad2<PK>(round_bf16x2(pre));
     return silu_grad2_accurate(pre);
 }
 
@@ -146,15 +147,18 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
     const int64_t nwarps = (int64_t)gridDim.x * SH::kWarps;
     const int64_t S = a.plan.S, C = a.plan.C, L = a.plan.L;
     const int64_t ncols = a.plan.ncols;
-#if !VCD_BWD_TMA
-    const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(a.x);
-    const __nv_bfloat16* __restrict__ dy = static_cast<const __nv_bfloat16*>(a.dy);
-#endif
     __nv_bfloat16* __restrict__ dx = static_cast<__nv_bfloat16*>(a.dx);
     const int32_t* __restrict__ cu = a.cu_seqlens;
     const int ncu = (int)(a.num_docs + 1);
     const int Ci = (int)C;                               // row stride, elements
     const bool with_bias = BIAS == kRouteRuntime ? a.bias_kind != kBiasNone : BIAS != kBiasNone;
+    // The mask-free path in packed FP32x2 instructions (two channels per
+    // instruction, the same rounding as two scalar ones, so the same bits)
+    // where that is faster, measured: the chunked shape and the deep shape
+    // without a bias (large fp32 2313 -> 2244 us, mid 80 -> 76 us); the wide
+    // shape and the masked paths run slower packed (register pressure).
+    constexpr bool kFastPk = kPK || SHAPE == kBwdChunked || (SHAPE == kBwdDeep && BIAS == kBiasNone);
+    constexpr bool kFastPa = kPA || kFastPk;
 
     // Assignment. Each column's units are cut into chunks of `per` consecutive
     // units (the plan's, from constants), and a warp streams a whole chunk as
@@ -174,14 +178,12 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
                           wid * kBwdNs * 8;
     uint32_t phases = 0;
     bool fault = false;
-    if (VCD_BWD_TMA) {
-        if (lane == 0) {
+    if (lane == 0) {
 #pragma unroll
-            for (int s = 0; s < kBwdNs; ++s) mbar_init(bars + 8 * s, 1);
-            mbar_init_fence();
-        }
-        __syncwarp();
+        for (int s = 0; s < kBwdNs; ++s) mbar_init(bars + 8 * s, 1);
+        mbar_init_fence();
     }
+    __syncwarp();
     for (int64_t asg = warp0; asg < n_asg; asg += nwarps) {
         const int64_t col = asg % ncols, chunk = asg / ncols;
         const int64_t row0 = chunk * per;
@@ -203,18 +205,9 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
 
         // The first batches' copies go out before the taps and the document
         // lookup, whose dependent loads then overlap them.
-#if !VCD_BWD_TMA
-        RowStream<2, kBwdRowBytes, int> rs;                 // x over [q0, u_end), dy over [t_begin, u_end)
-        {
-            const __nv_bfloat16* const bases[2] = {x, dy};
-            const int64_t lows[2] = {q0 > 0 ? q0 : 0, t_begin};
-            rs.init(bases, C, col, q0, lows, u_end, lane);
-        }
-#endif
 
         __syncwarp();                    // the previous unit's reads of the ring are done
         auto issue = [&](int i, int slot) {
-#if VCD_BWD_TMA
             // Tiles of tokens q0 + i U .. + U - 1 x the column's 128 channels
             // (rows outside [0, S) and channels past C arrive as zeros; the
             // x and dy rows outside what the unit uses are never read).
@@ -226,14 +219,6 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
                 tma_load_2d(st, &a.tmap_x, c, t, bar);
                 tma_load_2d(st + kBwdTensorBytes, &a.tmap_dy, c, t, bar);
             }
-#else
-            if (i < nb) {
-                const uint32_t st = ring_s + slot * kBwdStageBytes;
-                const uint32_t d[2] = {st, st + kBwdTensorBytes};
-                rs.stage<kBwdU>(d, i * kBwdU, x);
-            }
-            cp_async_commit();
-#endif
         };
 #pragma unroll
         for (int s = 0; s < kBwdNs - 1; ++s) issue(s, s);
@@ -456,15 +441,11 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
 
         int slot = 0;
         for (int i = 0; i < nb; ++i) {
-#if VCD_BWD_TMA
             if (!mbar_wait_bounded(bars + 8 * slot, (phases >> slot) & 1u)) {
                 fault = true;
                 break;
             }
             phases ^= 1u << slot;
-#else
-            cp_async_wait<kBwdNs - 2>();
-#endif
             __syncwarp();
             issue(i + kBwdNs - 1, slot == 0 ? kBwdNs - 1 : slot - 1);
             const int r0 = i * kBwdU;
@@ -512,20 +493,20 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
                     for (int p = 0; p < kNP; ++p) {
                         const float2 xf = bf16x2_to_float2(xv[p]);
                         const float2 gf = bf16x2_to_float2(gv[p]);
-                        float2 pre = fma2<kPK>(w[0][p], xc[0][p], b[p]);
-                        pre = fma2<kPK>(w[1][p], xc[1][p], pre);
-                        pre = fma2<kPK>(w[2][p], xc[2][p], pre);
-                        pre = fma2<kPK>(w[3][p], xf, pre);
-                        const float2 d = mul2<kPK>(gf, grad_at<POLICY>(pre));
-                        dw[0][p] = fma2<kPA>(d, xc[0][p], dw[0][p]);
-                        dw[1][p] = fma2<kPA>(d, xc[1][p], dw[1][p]);
-                        dw[2][p] = fma2<kPA>(d, xc[2][p], dw[2][p]);
-                        dw[3][p] = fma2<kPA>(d, xf, dw[3][p]);
-                        if (with_bias) db[p] = add2<kPA>(db[p], d);
-                        float2 g = mul2<kPA>(w[3][p], dc[0][p]);
-                        g = fma2<kPA>(w[2][p], dc[1][p], g);
-                        g = fma2<kPA>(w[1][p], dc[2][p], g);
-                        g = fma2<kPA>(w[0][p], d, g);
+                        float2 pre = fma2<kFastPk>(w[0][p], xc[0][p], b[p]);
+                        pre = fma2<kFastPk>(w[1][p], xc[1][p], pre);
+                        pre = fma2<kFastPk>(w[2][p], xc[2][p], pre);
+                        pre = fma2<kFastPk>(w[3][p], xf, pre);
+                        const float2 d = mul2<kFastPk>(gf, grad_at<POLICY, kFastPk>(pre));
+                        dw[0][p] = fma2<kFastPa>(d, xc[0][p], dw[0][p]);
+                        dw[1][p] = fma2<kFastPa>(d, xc[1][p], dw[1][p]);
+                        dw[2][p] = fma2<kFastPa>(d, xc[2][p], dw[2][p]);
+                        dw[3][p] = fma2<kFastPa>(d, xf, dw[3][p]);
+                        if (with_bias) db[p] = add2<kFastPa>(db[p], d);
+                        float2 g = mul2<kFastPa>(w[3][p], dc[0][p]);
+                        g = fma2<kFastPa>(w[2][p], dc[1][p], g);
+                        g = fma2<kFastPa>(w[1][p], dc[2][p], g);
+                        g = fma2<kFastPa>(w[0][p], d, g);
                         o[p] = float2_to_bf16x2(g);
                         xc[0][p] = xc[1][p];
                         xc[1][p] = xc[2][p];
@@ -638,10 +619,10 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
             slot = slot + 1 == kBwdNs ? 0 : slot + 1;
         }
 
-        if (VCD_BWD_TMA && fault) break;
+        if (fault) break;
         write_row();
     }
-    if (VCD_BWD_TMA && fault) {
+    if (fault) {
         // A tile never arrived: flag it, and give the stages still in flight
         // a bounded wait of their own before the warp leaves, so that no copy
         // lands in shared memory the CTA has released.
@@ -967,16 +948,11 @@ cudaError_t read_wait_fault(int* flag) {
 
 namespace {
 cudaError_t encode_maps(BwdArgs& a) {
-#if VCD_BWD_TMA
     const int rows = a.shape == kBwdWide ? BwdGeom<kBwdWide>::kU
                      : a.shape == kBwdDeep ? BwdGeom<kBwdDeep>::kU : BwdGeom<kBwdChunked>::kU;
     cudaError_t e = encode_bf16_rows(&a.tmap_x, a.x, a.plan.S, a.plan.C, kBwdColCh, rows);
     if (e == cudaSuccess) e = encode_bf16_rows(&a.tmap_dy, a.dy, a.plan.S, a.plan.C, kBwdColCh, rows);
     return e;
-#else
-    (void)a;
-    return cudaSuccess;
-#endif
 }
 }  // namespace
 
@@ -1017,12 +993,12 @@ cudaError_t launch_bwd(const BwdArgs& args, int sm_count, cudaStream_t stream) {
         {nullptr, launch_main_t<kBwdWide, false, kBiasF32, kPolicyBF16>, launch_main_t<kBwdWide, false, kBiasBF16, kPolicyBF16>},
         {nullptr, launch_main_t<kBwdWide, true, kBiasF32, kPolicyBF16>, launch_main_t<kBwdWide, true, kBiasBF16, kPolicyBF16>}};
     static const L deep_bf16[2][3] = {VCD_ROW(kBwdDeep, false, kPolicyBF16), VCD_ROW(kBwdDeep, true, kPolicyBF16)};
-    static const L fp32_t[2][3] = {VCD_ROW(VCD_FP32_SHAPE, false, kPolicyFP32),
-                                   VCD_ROW(VCD_FP32_SHAPE, true, kPolicyFP32)};
+    static const L fp32_t[2][3] = {VCD_ROW(kBwdChunked, false, kPolicyFP32),
+                                   VCD_ROW(kBwdChunked, true, kPolicyFP32)};
 #undef VCD_ROW
     const int wi = a.weight_bf16 ? 1 : 0;
     const bool fp32 = a.policy == kPolicyFP32;
-    const L fn = fp32 ? (a.shape == VCD_FP32_SHAPE ? fp32_t[wi][a.bias_kind] : nullptr)
+    const L fn = fp32 ? (a.shape == kBwdChunked ? fp32_t[wi][a.bias_kind] : nullptr)
                       : a.shape == kBwdWide ? wide_bf16[wi][a.bias_kind] : deep_bf16[wi][a.bias_kind];
     if (fn == nullptr) return cudaErrorInvalidValue;     // a shape bwd_shape never picks
     cudaError_t e = fn(a, sm_count, stream);

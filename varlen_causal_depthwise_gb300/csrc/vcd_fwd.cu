@@ -217,9 +217,10 @@ __global__ void __launch_bounds__(kThreadsPerCta, FwdGeom<SHAPE>::kCtas)
             __nv_bfloat16* yq = yp + (int64_t)r0 * ystep;
 
             if constexpr (SHAPE == kFwdExact) {
-                // every batch through one predicated path, each element
-                // checked; not unrolled (the instruction cache, measured)
-#pragma unroll 1
+                // every batch through one predicated path, each element checked
+                // (the repair out of line keeps the unrolled loop small enough
+                // for the instruction cache)
+#pragma unroll
                 for (int j = 0; j < kFwdU; ++j) {
                     const int r = r0 + j;
                     const uint2 xv = lds64(st + j * kFwdRowBytes);

@@ -70,22 +70,17 @@ inline int fwd_shape(int64_t S, int64_t num_docs) {
     return num_docs * kShortDocTokens >= S ? kFwdShortDocs : kFwdStream;
 }
 
-// The backward's launch shape for a call: deep for the "fp32" policy and for
-// short documents (instruction-heavy paths, where more warps hide more
-// latency); under the "bf16" policy with longer documents, deep when the route
-// has no bias -- those kernels keep all their state within 128 registers --
-// and wide with a bias, whose 16-warp kernels would spill registers. A
-// function of the call's arguments only, so a route's partial rows are the
-// same on every call and every device.
-#ifndef VCD_SHORT_DOCS_WIDE
-#define VCD_SHORT_DOCS_WIDE 0
-#endif
-#ifndef VCD_FP32_SHAPE
-#define VCD_FP32_SHAPE 2
-#endif
+// The backward's launch shape for a call: chunked for the "fp32" policy (its
+// 256-token units need the shared-memory chunk sums); under the "bf16"
+// policy deep for short documents (instruction-heavy masked paths, where more
+// warps hide more latency) and for routes without a bias (those kernels keep
+// all their state within 128 registers), wide with a bias on longer
+// documents, whose 16-warp kernels would spill. A function of the call's
+// arguments only, so a route's partial rows are the same on every call and
+// every device.
 inline int bwd_shape(int64_t S, int64_t num_docs, int policy, bool has_bias) {
-    if (policy == 1) return VCD_FP32_SHAPE;
-    if (!VCD_SHORT_DOCS_WIDE && num_docs * kShortDocTokens >= S) return kBwdDeep;
+    if (policy == 1) return kBwdChunked;
+    if (num_docs * kShortDocTokens >= S) return kBwdDeep;
     return has_bias ? kBwdWide : kBwdDeep;
 }
 
@@ -169,7 +164,7 @@ inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy, int sh
 // The most a policy's routes need over every call shape: the "fp32" policy
 // always runs the chunked shape, the "bf16" policy the wide or the deep one.
 inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy) {
-    if (policy == 1) return bwd_workspace_bytes_for(S, C, policy, VCD_FP32_SHAPE);
+    if (policy == 1) return bwd_workspace_bytes_for(S, C, policy, kBwdChunked);
     const uint64_t d = bwd_workspace_bytes_for(S, C, policy, kBwdDeep);
     const uint64_t w = bwd_workspace_bytes_for(S, C, policy, kBwdWide);
     return w > d ? w : d;
