@@ -67,9 +67,10 @@ def test_workspace_queries(lib):
     # one warp-sized unit per chunk, the larger of the two launch shapes (16
     # warps per SM: 48 columns x 50 rows = 2400 units)
     assert bf == 48 * 50 * 128 * 5 * 4
-    # "fp32": 256-token units (256 per column), 7 to a chunk so that the 38
-    # warps per column of the chunked shape each take about one: 37 chunks
-    assert fp == 48 * 37 * 128 * 5 * 4
+    # "fp32": 38 warps per column in the chunked shape, 7 units to a chunk
+    # (38 x 7 units of at most 256 tokens cover S), units of 248 tokens (the
+    # shortest multiple of 8 that covers S in 38 x 7): 265 units, 38 chunks
+    assert fp == 48 * 38 * 128 * 5 * 4
     with pytest.raises(ValueError):
         vcd.conv1d_bwd_route_workspace_size(8, 8, "fp16")
 
@@ -85,7 +86,7 @@ def test_call_workspace_query_follows_the_launch_shape(lib):
     assert call(S, C, 20, "bf16", False) == 48 * 50 * row          # deep: 2400 units
     assert call(S, C, S // 32, "bf16", True) == 48 * 50 * row      # short documents: deep
     assert call(S, C, S // 32 - 1, "bf16", True) == 48 * 38 * row
-    assert call(S, C, 20, "fp32", True) == call(S, C, 20, "fp32", False) == 48 * 37 * row  # chunks
+    assert call(S, C, 20, "fp32", True) == call(S, C, 20, "fp32", False) == 48 * 38 * row  # chunks
     for S_, C_, nd in ((4096, 256, 4), (131072, 1032, 52000), (300, 40, 3), (1, 8, 1)):
         for pol in ("bf16", "fp32"):
             for hb in (True, False):
@@ -242,9 +243,9 @@ def test_exact_workspace_query(lib):
         assert n > max(vcd.conv1d_bwd_call_workspace_size(S, C, 1, p, True) for p in ("bf16", "fp32"))
     # 65536 x 6144 in the chunked shape (1824 target warps): "bf16" 38 chunks
     # of 1725 tokens per column, lists of 1725 * 128 / 64 = 3450 entries;
-    # "fp32" 37 chunks of 7 units of 256 tokens, lists of 3584; the larger
+    # "fp32" 38 chunks of 7 units of 248 tokens, lists of 3472; the larger
     bf = 48 * 38 * (2560 + 3450 * 8 + 4)
-    fp = 48 * 37 * (2560 + 3584 * 8 + 4)
+    fp = 48 * 38 * (2560 + 3472 * 8 + 4)
     assert abs(vcd.conv1d_bwd_exact_workspace_size(65536, 6144) - max(bf, fp)) <= 32
     with pytest.raises(vcd.VcdError):
         vcd.conv1d_bwd_exact_workspace_size(8, 12)

@@ -73,8 +73,8 @@ def test_noalloc_refuses_shapes_beyond_its_scratch():
 
 
 def test_noalloc_fp32_policy_on_a_chunked_shape():
-    """The "fp32" policy at S = 65536, C = 6144: 256-token units folded seven
-    to a chunk, 1776 chunk rows of the fixed scratch's 3276."""
+    """The "fp32" policy at S = 65536, C = 6144: 248-token units folded seven
+    to a chunk, 1824 chunk rows of the fixed scratch's 3276."""
     S, C = 65536, 6144
     w = synth.make("linattn", device=DEV, S=S, C=C)
     ref = vcd.conv1d_bwd(w.x, w.dy, w.weight, w.cu_seqlens, w.bias, "fp32",

@@ -87,12 +87,10 @@ template <int SHAPE> struct BwdShapeT : BwdGeom<SHAPE> {
         return kSmemBytes + (SEG ? kAccBytes : 0) + kBarBytes;
     }
 };
-// Units of several per chunk are the "fp32" policy's, kFp32TokensPerUnit
-// tokens long; a multiple of the batch puts every unit boundary at the same
-// position of a batch.
-static_assert(kFp32TokensPerUnit % BwdGeom<kBwdDeep>::kU == 0, "unit boundaries must align");
-static_assert(kFp32TokensPerUnit % BwdGeom<kBwdChunked>::kU == 0, "unit boundaries must align");
-static_assert(BwdShapeT<kBwdDeep>::smem_bytes<true>() <= 227 * 1024, "accumulators do not fit");
+// Units of several per chunk are the "fp32" policy's, a multiple of
+// kFp32UnitAlign tokens long (vcd_plan.h); a multiple of the batch puts every
+// unit boundary at the same position of a batch.
+static_assert(kFp32UnitAlign % BwdGeom<kBwdChunked>::kU == 0, "unit boundaries must align");
 static_assert(BwdShapeT<kBwdChunked>::smem_bytes<true>() <= 227 * 1024, "accumulators do not fit");
 static_assert(BwdShapeT<kBwdWide>::smem_bytes<false>() <= 227 * 1024, "ring and barriers do not fit");
 
@@ -873,7 +871,7 @@ cudaError_t launch_main_form(const BwdArgs& a, int sm_count, cudaStream_t stream
 }
 
 // Chunks of several units come only from the "fp32" policy, which runs the
-// deep shape; every other route has one unit per chunk.
+// chunked shape; every other route has one unit per chunk.
 template <int SHAPE, bool W_BF16, int BIAS, int POLICY>
 cudaError_t launch_main_t(const BwdArgs& a, int sm_count, cudaStream_t stream) {
     if constexpr (SHAPE != kBwdWide && POLICY == kPolicyFP32) {

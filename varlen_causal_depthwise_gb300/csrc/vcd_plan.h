@@ -57,7 +57,7 @@ enum FwdShape { kFwdStream = 0, kFwdShortDocs = 1, kFwdExact = 2 };
 // bwd_shape() picks one per call.
 //   kBwdChunked: 12 warps, up to 168 registers, 8-token batches and room in
 //             shared memory for compensated per-chunk sums -- the "fp32"
-//             policy's chunks of 256-token units.
+//             policy's chunks of units of at most 256 tokens.
 enum BwdShape { kBwdWide = 0, kBwdDeep = 1, kBwdChunked = 2 };
 constexpr int kBwdShapeWarps[3] = {12, 16, 12};
 
@@ -71,7 +71,7 @@ inline int fwd_shape(int64_t S, int64_t num_docs) {
 }
 
 // The backward's launch shape for a call: chunked for the "fp32" policy (its
-// 256-token units need the shared-memory chunk sums); under the "bf16"
+// short units need the shared-memory chunk sums); under the "bf16"
 // policy deep for short documents (instruction-heavy masked paths, where more
 // warps hide more latency) and for routes without a bias (those kernels keep
 // all their state within 128 registers), wide with a bias on longer
@@ -136,6 +136,17 @@ inline Plan fwd_plan(int64_t S, int64_t C) { return make_plan(S, C, kFwdVec, kFw
 #endif
 constexpr int64_t kFp32TokensPerUnit = VCD_FP32_UNIT_TOKENS;
 
+// The chunk is sized first (units per chunk: the fewest that let each column's
+// warps cover S with units of at most kFp32TokensPerUnit tokens), then the
+// unit is the shortest multiple of kFp32UnitAlign tokens that lets the
+// column's chunks cover S: so each column gets close to its share of the
+// resident warps (a fixed 256-token unit left 15% of them idle at S = 131072
+// over 9 columns). Every unit but a column's last is L tokens long, L a
+// multiple of the chunked shape's batch so that unit boundaries fall at the
+// same position of a batch.
+constexpr int64_t kFp32UnitAlign = 8;
+static_assert(kFp32TokensPerUnit % kFp32UnitAlign == 0, "unit length must align");
+
 inline BwdPlan bwd_plan(int64_t S, int64_t C, int policy, int shape) {
     const int64_t warps = kGb300Sms * kBwdShapeWarps[shape];
     BwdPlan p;
@@ -143,11 +154,13 @@ inline BwdPlan bwd_plan(int64_t S, int64_t C, int policy, int shape) {
     p.per = 1;
     p.chunks = p.rows;
     if (policy == 1 && p.L > kFp32TokensPerUnit && S > 0) {
-        p.L = kFp32TokensPerUnit;
+        const int64_t wpc = warps / p.ncols > 0 ? warps / p.ncols : 1;   // warps per column
+        p.per = (S + wpc * kFp32TokensPerUnit - 1) / (wpc * kFp32TokensPerUnit);
+        const int64_t span = wpc * p.per;                                  // units per column at most
+        p.L = (S + span - 1) / span;
+        p.L = (p.L + kFp32UnitAlign - 1) / kFp32UnitAlign * kFp32UnitAlign;
         p.rows = (S + p.L - 1) / p.L;
         p.units = p.ncols * p.rows;
-        const int64_t wpc = warps / p.ncols > 0 ? warps / p.ncols : 1;   // warps per column
-        p.per = (p.rows + wpc - 1) / wpc;
         p.chunks = (p.rows + p.per - 1) / p.per;
     }
     return p;
