@@ -67,7 +67,7 @@ int conv1d_fwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
  * alone: the maximum over every route (bias or not, dtypes, policy, launch
  * shape) and the same on every device, so one buffer serves every call of
  * that shape: one row of 128 channels x 5 FP32 values (2560 bytes) per chunk
- * of work of each 128-channel column, at most max(2432, ceil(C / 128)) rows. The kernel
+ * of work of each 128-channel column, at most max(3072, ceil(C / 128)) rows. The kernel
  * writes every byte it later reads: the buffer needs no zeroing. Same errors
  * as the forward query. */
 int conv1d_bwd_workspace_size(int64_t S, int64_t C, size_t* bytes);
@@ -200,8 +200,8 @@ int conv1d_bwd_exact(const void* x, const void* dy, int64_t S, int64_t C,
 
 /* Size of the fixed device scratch used by conv1d_bwd_noalloc: 8 MiB. Under
  * either policy that holds the partial rows of every shape with
- * C <= 419328: at most max(2432, ceil(C / 128)) rows of 2560 bytes, i.e. at
- * most 6.2 MB while C <= 311296, and one row per 128-channel column above
+ * C <= 419328: at most max(3072, ceil(C / 128)) rows of 2560 bytes, i.e. at
+ * most 7.9 MB while C <= 393216, and one row per 128-channel column above
  * that. */
 #define VCD_NOALLOC_SCRATCH_BYTES (8u << 20)
 

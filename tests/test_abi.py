@@ -221,6 +221,9 @@ def test_noalloc_scratch_size_matches_the_header():
     (1 << 20, 419336, "fp32", False),
     (262144, 311296, "bf16", True),
     (262144, 8192, "fp32", True),       # 64 columns x 28 chunks
+    (1 << 20, 8, "bf16", True),         # transposed narrow column: at most 3072 rows
+    (1 << 20, 136, "fp32", True),
+    (1 << 20, 1032, "bf16", True),
     ((1 << 31) - 128, 6144, "fp32", True),
 ])
 def test_noalloc_limits_stated_in_the_header(lib, S, C, policy, fits):
@@ -229,6 +232,19 @@ def test_noalloc_limits_stated_in_the_header(lib, S, C, policy, fits):
     against VCD_NOALLOC_SCRATCH_BYTES."""
     need = vcd.conv1d_bwd_route_workspace_size(S, C, policy)
     assert (need <= NOALLOC_BYTES) == fits, (S, C, policy, need)
+
+
+def test_workspace_bound_stated_in_the_header(lib):
+    """conv1d_bwd_workspace_size never exceeds max(3072, ceil(C / 128)) rows of
+    2560 bytes (the bound include/vcd.h states), over shapes with and without
+    a narrow last column."""
+    rng = np.random.default_rng(5)
+    cases = [(S, C) for S in (1, 63, 4096, 131072, 1 << 20, 1 << 24)
+             for C in (8, 16, 40, 64, 72, 128, 136, 264, 1032, 2056, 8200, 65544)]
+    cases += [(int(rng.integers(1, 1 << 22)), 8 * int(rng.integers(1, 20000))) for _ in range(200)]
+    for S, C in cases:
+        rows = max(3072, -(-C // 128))
+        assert vcd.conv1d_bwd_workspace_size(S, C) <= rows * 2560, (S, C)
 
 
 def test_exact_workspace_query(lib):

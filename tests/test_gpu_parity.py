@@ -270,6 +270,45 @@ def test_recipes_full_size_sampled(name):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("S,C,docs,bias", [
+    (8000, 8200, ("uniform", 1, 3000, 0), torch.float32),    # "fp32": chunks of 2 units
+    (8000, 8200, ("uniform", 0, 5, 0), None),                # short documents, no bias
+    (30000, 2056, ("uniform", 0, 2000, 3), torch.bfloat16),  # "fp32": 14 transposed warps
+    (20000, 72, ("uniform", 0, 300, 1), torch.float32),      # 18 groups: not transposed
+    (20000, 40, ("uniform", 0, 9, 2), torch.float32),        # one column of 10 groups
+])
+def test_transposed_narrow_column(S, C, docs, bias):
+    """Shapes whose last 128-channel column holds at most 16 four-channel
+    groups: the backward transposes that column (several token pieces per
+    warp, a chunk's pieces added into its partial row). dx on every token of
+    the last column's channels and at random points, dweight / dbias on all
+    of the last column's channels and a sample of the others, both policies,
+    against the oracle at full size; and the bits repeat."""
+    rng = np.random.default_rng(S + C)
+    lengths = synth.doc_lengths(docs, S, rng)
+    w = synth.custom(S, C, lengths, seed=C, bias_dtype=bias, device=DEV)
+    xc, dyc, wgt, cu = w.x.cpu(), w.dy.cpu(), w.weight.cpu(), w.cu_seqlens.cpu()
+    bc = None if w.bias is None else w.bias.cpu()
+    last = np.arange(C - C % 128 if C % 128 else C - 128, C)
+    ts = np.concatenate([np.repeat(np.arange(S), len(last)), rng.integers(0, S, 4000)])
+    cs = np.concatenate([np.tile(last, S), rng.integers(0, C, 4000)])
+    chans = np.unique(np.concatenate([last, sample_channels(C, rng, 8)]))
+    tt, cc = torch.from_numpy(ts).to(DEV), torch.from_numpy(cs).to(DEV)
+    for pol in ("bf16", "fp32"):
+        dx, dW, dB, kw = run_grads(w, pol)
+        dx2, dW2, dB2 = run_bwd(w, pol, torch.float32, torch.float32)
+        torch.cuda.synchronize()
+        assert torch.equal(dx, dx2) and torch.equal(dW, dW2)
+        assert dB is None or torch.equal(dB, dB2)
+        rdx, adx = oracle.bwd_dx_at(xc, dyc, wgt, cu, ts, cs, bc, pol)
+        REPORT[f"narrow S={S} C={C} {pol} dx strict"] = bf16_close(
+            _np(dx[tt, cc]), rdx, adx, f"narrow S={S} C={C} {pol} dx")
+        rdw, rdb = oracle.bwd_params_at(xc, dyc, wgt, cu, chans, bc, pol)
+        check_grads(dW, dB, kw, rdw, rdb, pol, f"narrow S={S} C={C} {pol}", chans)
+    del w
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------- properties --
 
 @pytest.mark.parametrize("name", ["linattn", "boundary"])

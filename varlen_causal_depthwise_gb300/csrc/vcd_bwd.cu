@@ -130,7 +130,194 @@ constexpr float kExactGradErr = 0x1p-24f * 24.0f;
 // plus 2^-9 |v| stays below one ulp); larger error bounds are recomputed.
 constexpr float kExactAccept = 0x1p-9f;
 
-template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG, bool EXACT = false>
+// The transposed narrow column (vcd_plan.h, narrow_plan): assignment k of
+// that column. Lane gi + g s (g = the column's four-channel groups) takes
+// group gi of piece s % h of chunk k q + s / h, a stretch of P tokens that it
+// walks alone: its own copies of x and dy (8-byte cp.async into its bytes of
+// the warp's ring, the layout of a full column's stage), its own cu_seqlens
+// cursor, and every token through one branch-free path (the main loop's
+// arithmetic, each term selected by operand). At the end the lanes of a
+// chunk's later pieces hand their five FP32 sums per channel to the chunk's
+// first piece, which adds them in piece order (compensated when the chunk
+// holds several units, the "fp32" policy's) and writes the chunk's partial
+// row. Out of line: the main loop's register allocation stays as it is.
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY>
+__device__ __noinline__ void bwd_narrow(const BwdArgs& a, int64_t k, uint32_t ring_s,
+                                        const unsigned char* ring, int lane) {
+    using SH = BwdShapeT<SHAPE>;
+    constexpr int kU = SH::kU, kNs = SH::kNs;
+    const int64_t S = a.plan.S, C = a.plan.C;
+    const int g = (int)a.plan.ng, h = (int)a.plan.h, nq = (int)a.plan.q;
+    const int gi = lane % g, s = lane / g;
+    const int64_t chunk = k * nq + s / h;
+    const int piece = s % h;
+    const bool valid = s < nq * h && chunk < a.plan.chunks;
+    const int64_t c0 = a.plan.nfull * kBwdColCh + gi * kBwdVec;
+    const int64_t span = a.plan.per * a.plan.L;                 // tokens of a chunk
+    const int64_t P = (span + h - 1) / h;                       // of a piece
+    int64_t t0 = 0, t1 = 0;
+    if (valid) {
+        const int64_t cs = chunk * span, ce = cs + span < S ? cs + span : S;
+        t0 = cs + piece * P < ce ? cs + piece * P : ce;
+        t1 = t0 + P < ce ? t0 + P : ce;
+    }
+    // relative tokens r (token q0 + r), as in the main loop: dweight and dx
+    // for r in [3, r_end); x read over [q0, t_du), dy over [t0, t_du) (dpre
+    // of the three tokens after the piece enters its last dx)
+    const int64_t q0 = t0 - 3;
+    const int64_t t_du = valid ? (t1 + 3 < S ? t1 + 3 : S) : 0;
+    const int r_end = (int)(t1 - q0);
+    const int nb = (int)((P + 6 + kU - 1) / kU);                // warp-uniform
+    const bool with_bias = BIAS == kRouteRuntime ? a.bias_kind != kBiasNone : BIAS != kBiasNone;
+    const int32_t* __restrict__ cu = a.cu_seqlens;
+    const int ncu = (int)(a.num_docs + 1);
+
+    const unsigned char* const xg = static_cast<const unsigned char*>(a.x) + (q0 * C + c0) * 2;
+    const unsigned char* const gg = static_cast<const unsigned char*>(a.dy) + (q0 * C + c0) * 2;
+    const int64_t rowb = C * 2;
+    auto issue = [&](int i, int slot) {
+        if (i < nb) {
+            const uint32_t st = ring_s + slot * SH::kStageBytes + lane * (2 * kBwdVec);
+#pragma unroll
+            for (int j = 0; j < kU; ++j) {
+                const int r = i * kU + j;
+                const int64_t t = q0 + r;
+                const bool okx = valid && t >= 0 && t < t_du;
+                const bool okg = okx && r >= 3;
+                const int64_t off = (int64_t)r * rowb;
+                cp_async8(st + j * kBwdRowBytes, okx ? xg + off : a.x, okx);
+                cp_async8(st + SH::kTensorBytes + j * kBwdRowBytes, okg ? gg + off : a.dy, okg);
+            }
+        }
+        cp_async_commit();
+    };
+    __syncwarp();                        // the previous assignment's reads of the ring are done
+#pragma unroll
+    for (int i = 0; i < kNs - 1; ++i) issue(i, i);
+
+    float2 w[4][kNP], b[kNP];
+    if constexpr (BIAS == kRouteRuntime)
+        load_taps_rt(a.weight, a.bias, a.weight_bf16 != 0, a.bias_kind, c0, valid, w, b);
+    else
+        load_taps<W_BF16, BIAS, kNP>(a.weight, a.bias, c0, valid, w, b);
+    LaneDocs doc;
+    doc.init(cu, ncu, (int)q0 - 2);
+    uint32_t carry = doc.starts(cu, ncu, (int)q0 - 2, 2);               // bits of q0-2, q0-1
+
+    float2 xc[3][kNP], dc[3][kNP], dw[4][kNP], db[kNP];
+#pragma unroll
+    for (int p = 0; p < kNP; ++p) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) xc[j][p] = dc[j][p] = zero2();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dw[j][p] = zero2();
+        db[p] = zero2();
+    }
+    __nv_bfloat16* dxq = static_cast<__nv_bfloat16*>(a.dx) + (q0 - 3) * C + c0;   // token q0 - 3
+
+    int slot = 0;
+    for (int i = 0; i < nb; ++i) {
+        cp_async_wait<kNs - 2>();        // this lane's copies of batch i have landed
+        __syncwarp();
+        issue(i + kNs - 1, slot == 0 ? kNs - 1 : slot - 1);
+        const int r0 = i * kU;
+        const uint32_t nw = doc.starts(cu, ncu, (int)(q0 + r0), kU);
+        const uint32_t M = carry | (nw << 2);                            // bit i <-> token q - 2 + i
+        carry = nw >> (kU - 2);
+        const unsigned char* sx = ring + slot * SH::kStageBytes + lane * (2 * kBwdVec);
+        const unsigned char* sg = sx + SH::kTensorBytes;
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+            const int r = r0 + j;
+            uint32_t xv[kNP], gv[kNP], o[kNP];
+            lds_pairs<kBwdVec>(sx + j * kBwdRowBytes, xv);
+            lds_pairs<kBwdVec>(sg + j * kBwdRowBytes, gv);
+            // The lanes' masks differ (each walks its own tokens), so every
+            // term is selected by operand, never branched around: a term
+            // outside the document or the piece multiplies a selected zero
+            // (same values as skipping it, whatever the excluded x or dy
+            // holds). dy is zero-filled outside [t0, t_du), so dpre there is 0.
+            const bool m1 = !bit(M, j + 2);
+            const bool m2 = m1 && !bit(M, j + 1);
+            const bool m3 = m2 && !bit(M, j);
+            const bool k1 = !bit(M, j);
+            const bool k2 = k1 && !bit(M, j + 1);
+            const bool k3 = k2 && !bit(M, j + 2);
+            const bool acc = r >= 3 && r < r_end;
+            const bool emit = r >= 6 && r - 3 < r_end;
+#pragma unroll
+            for (int p = 0; p < kNP; ++p) {
+                const float2 xf = bf16x2_to_float2(xv[p]);
+                const float2 gf = bf16x2_to_float2(gv[p]);
+                const float2 x0 = m3 ? xc[0][p] : zero2();
+                const float2 x1 = m2 ? xc[1][p] : zero2();
+                const float2 x2 = m1 ? xc[2][p] : zero2();
+                float2 pre = fma2<true>(w[0][p], x0, b[p]);
+                pre = fma2<true>(w[1][p], x1, pre);
+                pre = fma2<true>(w[2][p], x2, pre);
+                pre = fma2<true>(w[3][p], xf, pre);
+                const float2 d = mul2<true>(gf, grad_at<POLICY, true>(pre));
+                const float2 da = acc ? d : zero2();
+                dw[0][p] = fma2<true>(da, x0, dw[0][p]);
+                dw[1][p] = fma2<true>(da, x1, dw[1][p]);
+                dw[2][p] = fma2<true>(da, x2, dw[2][p]);
+                dw[3][p] = fma2<true>(da, xf, dw[3][p]);
+                if (with_bias) db[p] = add2<true>(db[p], da);
+                const float2 e1 = k1 ? dc[1][p] : zero2();
+                const float2 e2 = k2 ? dc[2][p] : zero2();
+                const float2 e3 = k3 ? d : zero2();
+                float2 gsum = mul2<true>(w[3][p], dc[0][p]);
+                gsum = fma2<true>(w[2][p], e1, gsum);
+                gsum = fma2<true>(w[1][p], e2, gsum);
+                gsum = fma2<true>(w[0][p], e3, gsum);
+                o[p] = float2_to_bf16x2(gsum);
+                xc[0][p] = xc[1][p];
+                xc[1][p] = xc[2][p];
+                xc[2][p] = xf;
+                dc[0][p] = dc[1][p];
+                dc[1][p] = dc[2][p];
+                dc[2][p] = d;
+            }
+            if (emit) st_pairs<kBwdVec>(dxq + (int64_t)r * C, o);
+        }
+        slot = slot + 1 == kNs ? 0 : slot + 1;
+    }
+    cp_async_wait<0>();                  // nothing in flight into the ring past this point
+
+    // The chunk's row: pieces 1 .. h-1 (lanes lane + g, lane + 2g, ...) added
+    // into piece 0's sums in piece order. Units of the "fp32" policy's chunks
+    // go through a compensated sum, as the main loop's chunks do.
+    const bool comp = a.plan.per > 1;
+    float own[kPartialStride * kBwdVec], hi[kPartialStride * kBwdVec], lo[kPartialStride * kBwdVec];
+#pragma unroll
+    for (int f = 0; f < kPartialStride * kBwdVec; ++f) {
+        const int ch = f / kPartialStride, kk = f % kPartialStride;
+        const float2 v = kk < 4 ? dw[kk][ch / 2] : db[ch / 2];
+        own[f] = hi[f] = (ch & 1) ? v.y : v.x;
+        lo[f] = 0.0f;
+    }
+    for (int j = 1; j < h; ++j) {
+        const int src = lane + j * g < 32 ? lane + j * g : lane;
+#pragma unroll
+        for (int f = 0; f < kPartialStride * kBwdVec; ++f) {
+            const float v = __shfl_sync(kFull, own[f], src);
+            if (comp) acc_two_sum(hi[f], lo[f], v);
+            else hi[f] = __fadd_rn(hi[f], v);
+        }
+    }
+    if (valid && piece == 0) {
+        float2* dst = reinterpret_cast<float2*>(
+            a.partials + ((chunk * a.plan.ncols + a.plan.nfull) * kBwdColCh + gi * kBwdVec) * kPartialStride);
+#pragma unroll
+        for (int f = 0; f < kPartialStride * kBwdVec / 2; ++f)
+            dst[f] = make_float2(__fadd_rn(hi[2 * f], lo[2 * f]), __fadd_rn(hi[2 * f + 1], lo[2 * f + 1]));
+    }
+}
+
+// NARROW: the plan transposes the last column (a.plan.nnarrow > 0); its
+// assignments run bwd_narrow. A separate instantiation, so that the other
+// kernels' register allocation does not carry that path.
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG, bool EXACT = false, bool NARROW = false>
 __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
     bwd_main_kernel(const __grid_constant__ BwdArgs a) {
     using SH = BwdShapeT<SHAPE>;
@@ -167,7 +354,9 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
     // computes it. Without SEG every chunk is one unit.
     const int64_t rows = a.plan.rows;
     const int64_t per = SEG ? a.plan.per : 1;
-    const int64_t n_asg = ncols * a.plan.chunks;
+    const int64_t nfull = NARROW ? a.plan.nfull : ncols;
+    const int64_t n_full_asg = nfull * a.plan.chunks;           // then the transposed column's
+    const int64_t n_asg = NARROW ? n_full_asg + a.plan.nnarrow : n_full_asg;
     float* const acc = reinterpret_cast<float*>(smem + SH::kSmemBytes) +
                        wid * SH::kAccFloats * 32 + lane;        // SEG: [value][lane] of this warp
     // TMA ring: this warp's stage barriers, initialised once (one arrival per
@@ -183,7 +372,21 @@ __global__ void __launch_bounds__(BwdShapeT<SHAPE>::kThreads, 1)
     }
     __syncwarp();
     for (int64_t asg = warp0; asg < n_asg; asg += nwarps) {
-        const int64_t col = asg % ncols, chunk = asg / ncols;
+        // The transposed column's assignments sit evenly spaced among the
+        // others (one in `stride`), so that no SM holds more than one of
+        // their warps: their lanes' scattered 8-byte copies and stores load
+        // the SM's L1 several times more per token than a full column's.
+        int64_t fa = asg;                                        // full-column assignment
+        if constexpr (NARROW) {
+            const int64_t nn = a.plan.nnarrow, stride = n_asg / nn;
+            const int64_t ks = asg / stride;
+            if (asg % stride == 0 && ks < nn) {
+                bwd_narrow<SHAPE, W_BF16, BIAS, POLICY>(a, ks, ring_s, ring, lane);
+                continue;
+            }
+            fa = asg - (ks + 1 < nn ? ks + 1 : nn);
+        }
+        const int64_t col = fa % nfull, chunk = fa / nfull;
         const int64_t row0 = chunk * per;
         const int64_t row1 = !SEG ? row0 + 1 : row0 + per < rows ? row0 + per : rows;
         const int64_t c0 = col * kBwdColCh + lane * kBwdVec;
@@ -830,7 +1033,7 @@ __global__ void __launch_bounds__(256) bwd_exact_fixup_kernel(const BwdArgs a) {
 
 // -------------------------------------------------------------- launch ---
 
-template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG, bool EXACT = false>
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG, bool EXACT = false, bool NARROW = false>
 int prepare_main_t() {
     // Once per (instantiation, device): allow the dynamic shared memory and
     // read the occupancy; both are host-side queries. The cache entries are
@@ -842,23 +1045,24 @@ int prepare_main_t() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     const int known = occ[dev].load(std::memory_order_relaxed);
     if (known > 0) return known;
-    if (cudaFuncSetAttribute(bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT>,
+    if (cudaFuncSetAttribute(bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT, NARROW>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT, NARROW>,
                                                       SH::kThreads, kSmem) != cudaSuccess)
         return 0;
     occ[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
-template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG, bool EXACT = false>
+template <int SHAPE, bool W_BF16, int BIAS, int POLICY, bool SEG, bool EXACT = false, bool NARROW = false>
 cudaError_t launch_main_form(const BwdArgs& a, int sm_count, cudaStream_t stream) {
     using SH = BwdShapeT<SHAPE>;
-    const int occ = prepare_main_t<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT>();
+    if ((a.plan.nnarrow > 0) != NARROW) return cudaErrorInvalidValue;
+    const int occ = prepare_main_t<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT, NARROW>();
     if (occ <= 0) return cudaErrorInvalidConfiguration;
-    const int64_t n_asg = a.plan.ncols * a.plan.chunks;
+    const int64_t n_asg = a.plan.nfull * a.plan.chunks + a.plan.nnarrow;
     const int64_t ctas_needed = (n_asg + SH::kWarps - 1) / SH::kWarps;
     const int64_t resident = (int64_t)sm_count * occ;
     const int64_t grid = ctas_needed < resident ? ctas_needed : resident;
@@ -867,18 +1071,23 @@ cudaError_t launch_main_form(const BwdArgs& a, int sm_count, cudaStream_t stream
     cfg.blockDim = dim3(SH::kThreads);
     cfg.dynamicSmemBytes = SH::template smem_bytes<SEG>();
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT>, a);
+    return cudaLaunchKernelEx(&cfg, bwd_main_kernel<SHAPE, W_BF16, BIAS, POLICY, SEG, EXACT, NARROW>, a);
 }
 
 // Chunks of several units come only from the "fp32" policy, which runs the
 // chunked shape; every other route has one unit per chunk.
+// Plans with the transposed narrow column take the NARROW instantiations.
 template <int SHAPE, bool W_BF16, int BIAS, int POLICY>
 cudaError_t launch_main_t(const BwdArgs& a, int sm_count, cudaStream_t stream) {
+    const bool narrow = a.plan.nnarrow > 0;
     if constexpr (SHAPE != kBwdWide && POLICY == kPolicyFP32) {
-        if (a.plan.per > 1) return launch_main_form<SHAPE, W_BF16, BIAS, POLICY, true>(a, sm_count, stream);
+        if (a.plan.per > 1)
+            return narrow ? launch_main_form<SHAPE, W_BF16, BIAS, POLICY, true, false, true>(a, sm_count, stream)
+                          : launch_main_form<SHAPE, W_BF16, BIAS, POLICY, true>(a, sm_count, stream);
     }
     if (a.plan.per > 1) return cudaErrorInvalidValue;
-    return launch_main_form<SHAPE, W_BF16, BIAS, POLICY, false>(a, sm_count, stream);
+    return narrow ? launch_main_form<SHAPE, W_BF16, BIAS, POLICY, false, false, true>(a, sm_count, stream)
+                  : launch_main_form<SHAPE, W_BF16, BIAS, POLICY, false>(a, sm_count, stream);
 }
 
 template <bool COMP>

@@ -224,7 +224,7 @@ int bwd_call(const void* x, const void* dy, int64_t S, int64_t C, const void* we
     a.dweight_bf16 = dweight_dtype == VCD_BF16;
     a.dbias_bf16 = dbias_dtype == VCD_BF16;
     a.shape = shape;
-    a.plan = vcd::bwd_plan(S, C, policy, shape);
+    a.plan = vcd::bwd_plan(S, C, policy, shape, !exact);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     a.xlist = exact ? reinterpret_cast<uint64_t*>(ws + xl.list_offset) : nullptr;
     a.xcount = exact ? reinterpret_cast<uint32_t*>(ws + xl.count_offset) : nullptr;

@@ -101,6 +101,13 @@ struct Plan {
 struct BwdPlan : Plan {
     int64_t per;      // units per chunk
     int64_t chunks;   // chunks per column
+    // The transposed narrow column (below); nfull == ncols and nnarrow == 0
+    // when the last column runs like the others.
+    int64_t nfull;    // columns in the normal mapping: chunk c of column k is assignment c nfull + k
+    int64_t ng;       // four-channel groups of the transposed column
+    int64_t h;        // pieces per chunk of the transposed column
+    int64_t q;        // its chunks per warp
+    int64_t nnarrow;  // its warps: assignments nfull chunks .. + nnarrow - 1
 };
 
 inline Plan make_plan(int64_t S, int64_t C, int vec, int64_t target_units) {
@@ -147,12 +154,95 @@ constexpr int64_t kFp32TokensPerUnit = VCD_FP32_UNIT_TOKENS;
 constexpr int64_t kFp32UnitAlign = 8;
 static_assert(kFp32TokensPerUnit % kFp32UnitAlign == 0, "unit length must align");
 
-inline BwdPlan bwd_plan(int64_t S, int64_t C, int policy, int shape) {
+// The narrow last column. When C's last 128-channel column holds g <= 16 of
+// its 32 four-channel groups, a warp on it in the normal mapping costs as
+// much per token as on a full column for g/32 of the data (C = 1032: 1/9 of
+// the warp time for 1/129 of the elements). The backward transposes that
+// column: a warp covers m = 32/g stretches ("pieces") of its tokens at once,
+// g lanes on each, one per group. A chunk of the column is cut into h equal
+// pieces (below), a warp takes q = m/h whole chunks and adds each chunk's
+// pieces in piece order into the chunk's partial row. Those few warps take the whole column, and the full columns
+// share the rest of the resident warps. The partial rows keep their layout
+// (chunks x ncols rows); a transposed plan is capped at kMaxPartialRows of
+// them.
+constexpr int64_t kNarrowMaxGroups = 16;
+constexpr int64_t kMaxPartialRows = 3072;
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The transposed plan for the last column's g groups, or false (p untouched)
+// where none applies.
+inline bool narrow_plan(BwdPlan& p, int64_t S, int64_t warps, int policy, int64_t g) {
+    const int64_t m = 32 / g, nfull = p.ncols - 1;
+    const int64_t row_cap = kMaxPartialRows / p.ncols;          // chunks per column at most
+    const int64_t tok_cap = ceil_div(S, kMinTokensPerUnit);
+    if (row_cap < 1) return false;
+    // chunks per column W with W nfull + W / qq <= warps
+    auto share = [&](int64_t qq) {
+        const int64_t w = warps * qq / (nfull * qq + 1);
+        return w < 1 ? 1 : w > row_cap ? row_cap : w;
+    };
+    // pieces per chunk: the smallest multiple of the chunk's units that is at
+    // least 4 under the "bf16" policy, 6 under "fp32" (a transposed lane
+    // takes about four times a full column lane's time per token, more with
+    // the accurate SiLU'; measured), else the largest multiple that fits m
+    const int64_t h_min = policy == 1 ? 6 : 4;
+    auto pieces = [&](int64_t per) -> int64_t {
+        int64_t h = (h_min + per - 1) / per * per;
+        while (h > m && h > per) h -= per;
+        return h;
+    };
+    // the plan for a target of wpc chunks per column
+    auto make = [&](int64_t wpc, BwdPlan& r) -> bool {
+        r = p;
+        r.per = policy == 1 ? ceil_div(S, wpc * kFp32TokensPerUnit) : 1;
+        const int64_t h = pieces(r.per);
+        if (m / h < 1) return false;
+        if (r.per > 1) {
+            r.L = ceil_div(ceil_div(S, wpc * r.per), kFp32UnitAlign) * kFp32UnitAlign;
+            r.rows = ceil_div(S, r.L);
+            r.chunks = ceil_div(r.rows, r.per);
+        } else {
+            const int64_t rows = wpc < tok_cap ? wpc : tok_cap;
+            r.L = ceil_div(S, rows);
+            r.rows = ceil_div(S, r.L);
+            r.chunks = r.rows;
+        }
+        r.units = r.ncols * r.rows;
+        r.nfull = nfull;
+        r.ng = g;
+        r.h = h;
+        r.q = m / h;
+        r.nnarrow = ceil_div(r.chunks, r.q);
+        return true;
+    };
+    // the most chunks per column whose assignments fit the resident warps,
+    // from the estimate down
+    BwdPlan r;
+    int64_t wpc = share(m / pieces(1));
+    for (;; --wpc) {
+        if (!make(wpc, r)) return false;
+        if (r.nfull * r.chunks + r.nnarrow <= warps || wpc == 1) break;
+    }
+    p = r;
+    return true;
+}
+
+// transpose: allow the transposed narrow column (the exactness-guarded route
+// keeps the normal mapping).
+inline BwdPlan bwd_plan(int64_t S, int64_t C, int policy, int shape, bool transpose = true) {
     const int64_t warps = kGb300Sms * kBwdShapeWarps[shape];
     BwdPlan p;
     static_cast<Plan&>(p) = make_plan(S, C, kBwdVec, warps);
     p.per = 1;
     p.chunks = p.rows;
+    p.nfull = p.ncols;
+    p.ng = 0;
+    p.h = 1;
+    p.q = 0;
+    p.nnarrow = 0;
+    const int64_t g = p.groups - 32 * (p.ncols - 1);             // groups of the last column
+    if (transpose && S > 0 && g <= kNarrowMaxGroups && narrow_plan(p, S, warps, policy, g)) return p;
     if (policy == 1 && p.L > kFp32TokensPerUnit && S > 0) {
         const int64_t wpc = warps / p.ncols > 0 ? warps / p.ncols : 1;   // warps per column
         p.per = (S + wpc * kFp32TokensPerUnit - 1) / (wpc * kFp32TokensPerUnit);
@@ -168,9 +258,10 @@ inline BwdPlan bwd_plan(int64_t S, int64_t C, int policy, int shape) {
 
 // Bytes of one route's partial rows: one FP32 row of 32 * kBwdVec channels x
 // 5 values per chunk of each column.
-inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy, int shape) {
+inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy, int shape,
+                                        bool transpose = true) {
     if (S <= 0) return 0;
-    const BwdPlan p = bwd_plan(S, C, policy, shape);
+    const BwdPlan p = bwd_plan(S, C, policy, shape, transpose);
     return (uint64_t)p.chunks * p.ncols * p.col_channels * kPartialStride * sizeof(float);
 }
 
@@ -207,10 +298,10 @@ struct ExactLayout {
 inline ExactLayout exact_layout(int64_t S, int64_t C, int policy) {
     ExactLayout e = {0, 0, 0, 0, 0};
     if (S <= 0) return e;
-    const BwdPlan p = bwd_plan(S, C, policy, kBwdChunked);
+    const BwdPlan p = bwd_plan(S, C, policy, kBwdChunked, false);
     const uint64_t lists = (uint64_t)p.chunks * p.ncols;
     e.cap = exact_list_cap(p);
-    e.partial_bytes = round16(bwd_workspace_bytes_for(S, C, policy, kBwdChunked));
+    e.partial_bytes = round16(bwd_workspace_bytes_for(S, C, policy, kBwdChunked, false));
     e.list_offset = e.partial_bytes;
     e.count_offset = round16(e.list_offset + lists * (uint64_t)e.cap * 8);
     e.total = round16(e.count_offset + lists * 4);
