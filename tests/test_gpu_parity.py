@@ -280,10 +280,10 @@ def test_recipes_full_size_sampled(name):
 def test_transposed_narrow_column(S, C, docs, bias):
     """Shapes whose last 128-channel column holds at most 16 four-channel
     groups: the backward transposes that column (several token pieces per
-    warp, a chunk's pieces added into its partial row). dx on every token of
-    the last column's channels and at random points, dweight / dbias on all
-    of the last column's channels and a sample of the others, both policies,
-    against the oracle at full size; and the bits repeat."""
+    warp, a chunk's pieces added into its partial row). y and dx on every
+    token of the last column's channels and at random points, dweight /
+    dbias on all of the last column's channels and a sample of the others,
+    both policies, against the oracle at full size; and the bits repeat."""
     rng = np.random.default_rng(S + C)
     lengths = synth.doc_lengths(docs, S, rng)
     w = synth.custom(S, C, lengths, seed=C, bias_dtype=bias, device=DEV)
@@ -294,6 +294,12 @@ def test_transposed_narrow_column(S, C, docs, bias):
     cs = np.concatenate([np.tile(last, S), rng.integers(0, C, 4000)])
     chans = np.unique(np.concatenate([last, sample_channels(C, rng, 8)]))
     tt, cc = torch.from_numpy(ts).to(DEV), torch.from_numpy(cs).to(DEV)
+    y = run_fwd(w)
+    torch.cuda.synchronize()
+    assert torch.equal(y, run_fwd(w))
+    ry, ay = oracle.fwd_at(xc, wgt, cu, ts, cs, bc)
+    REPORT[f"narrow S={S} C={C} y strict"] = bf16_close(_np(y[tt, cc]), ry, ay, f"narrow S={S} C={C} y")
+    del y
     for pol in ("bf16", "fp32"):
         dx, dW, dB, kw = run_grads(w, pol)
         dx2, dW2, dB2 = run_bwd(w, pol, torch.float32, torch.float32)

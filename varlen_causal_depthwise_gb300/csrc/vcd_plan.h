@@ -161,10 +161,12 @@ static_assert(kFp32TokensPerUnit % kFp32UnitAlign == 0, "unit length must align"
 // column: a warp covers m = 32/g stretches ("pieces") of its tokens at once,
 // g lanes on each, one per group. A chunk of the column is cut into h equal
 // pieces (below), a warp takes q = m/h whole chunks and adds each chunk's
-// pieces in piece order into the chunk's partial row. Those few warps take the whole column, and the full columns
-// share the rest of the resident warps. The partial rows keep their layout
-// (chunks x ncols rows); a transposed plan is capped at kMaxPartialRows of
-// them.
+// pieces in piece order into the chunk's partial row. Those few warps take
+// the whole column, and the full columns share the rest of the resident
+// warps. The partial rows keep their layout (chunks x ncols rows); a
+// transposed plan is capped at kMaxPartialRows of them. (The forward keeps
+// the normal mapping: a transposed forward measured slower, its lanes'
+// scattered 8-byte loads and stores costing more than the idle lanes.)
 constexpr int64_t kNarrowMaxGroups = 16;
 constexpr int64_t kMaxPartialRows = 3072;
 
