@@ -150,18 +150,6 @@ __global__ void __launch_bounds__(kThreadsPerCta, FwdGeom<SHAPE>::kCtas)
         const int n_rel = (int)(t_end - q0);                    // relative tokens 0 .. n_rel-1
         const int nb = (n_rel + kFwdU - 1) / kFwdU;
 
-        float2 w[4][2], b[2];
-        if (BIAS == kRouteRuntime)
-            load_taps_rt(a.weight, a.bias, a.weight_bf16 != 0, a.bias_kind, c0, active, w, b);
-        else
-            load_taps<W_BF16, BIAS, 2>(a.weight, a.bias, c0, active, w, b);
-        DocCursor doc;
-        doc.init(cu, ncu, (int)q0 - 2, lane);
-        uint32_t carry = doc.starts(cu, ncu, (int)q0 - 2, 2, lane);            // bits of q0-2, q0-1
-        float2 xc[3][2];                                              // x[q-3], x[q-2], x[q-1]
-#pragma unroll
-        for (int k = 0; k < 3; ++k) xc[k][0] = xc[k][1] = zero2();
-
         RowStream<1, kFwdRowBytes, int64_t> rs;
         if (!kTma) {
             const __nv_bfloat16* const bases[1] = {x};
@@ -191,9 +179,29 @@ __global__ void __launch_bounds__(kThreadsPerCta, FwdGeom<SHAPE>::kCtas)
         __nv_bfloat16* yp = y + q0 * C + c0;                   // y row of relative token 0
         const int64_t ystep = C;
 
+        // The taps and the document lookup (a chain of dependent loads) go
+        // after the first batches' copies, whose latency they then overlap;
+        // the exact shape keeps them first (its registers are tighter).
+        float2 w[4][2], b[2];
+        DocCursor doc;
+        uint32_t carry;
+        auto setup = [&]() {
+            if (BIAS == kRouteRuntime)
+                load_taps_rt(a.weight, a.bias, a.weight_bf16 != 0, a.bias_kind, c0, active, w, b);
+            else
+                load_taps<W_BF16, BIAS, 2>(a.weight, a.bias, c0, active, w, b);
+            doc.init(cu, ncu, (int)q0 - 2, lane);
+            carry = doc.starts(cu, ncu, (int)q0 - 2, 2, lane);               // bits of q0-2, q0-1
+        };
+        if constexpr (SHAPE == kFwdExact) setup();
         __syncwarp();                    // the previous unit's reads of the ring are done
 #pragma unroll
         for (int s = 0; s < kFwdNs - 1; ++s) issue(s, s);
+        if constexpr (SHAPE != kFwdExact) setup();
+        float2 xc[3][2];                                              // x[q-3], x[q-2], x[q-1]
+#pragma unroll
+        for (int k = 0; k < 3; ++k) xc[k][0] = xc[k][1] = zero2();
+
 
         int slot = 0;                    // ring stage of batch i
         for (int i = 0; i < nb; ++i) {
