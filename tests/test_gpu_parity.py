@@ -195,7 +195,7 @@ def _unit_edges(S, C, vec, target_units):
     """Token positions next to work-unit edges (sample selection only; mirrors
     the unit map: vec channels per lane, 32 lanes per column)."""
     ncols = -(-(C // vec) // 32)
-    rows = max(1, min(target_units // ncols, -(-S // 64)))
+    rows = max(1, min(target_units // ncols, -(-S // 16)))
     L = -(-S // rows)
     edges = np.arange(0, S, L)
     return np.unique(np.clip(np.concatenate([edges + d for d in (-4, -3, -1, 0, 1, 2, 3)]), 0, S - 1))

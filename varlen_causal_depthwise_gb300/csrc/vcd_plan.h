@@ -27,7 +27,12 @@ constexpr int kThreadsPerCta = 32 * kWarpsPerCta;
 #endif
 constexpr int kFwdVec = 4;                    // channels per lane, forward
 constexpr int kBwdVec = VCD_BWD_VEC;          // channels per lane, backward
-constexpr int64_t kMinTokensPerUnit = 64;     // keeps the 3-token halo below 5%
+// The shortest unit a plan cuts: it binds only where S is small against the
+// resident warps (fewer than 16 tokens per warp), where the time is latency
+// and the parallelism counts for more than the 3-token halo's extra reads
+// (4096 x 256: forward 16 -> 10 us, backward 30 -> 21 us against 64-token
+// units, measured).
+constexpr int64_t kMinTokensPerUnit = 16;
 constexpr int kPartialStride = 5;             // dweight[0..3], dbias per channel
 
 #ifndef VCD_FWD_CTAS_PER_SM
