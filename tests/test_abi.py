@@ -78,13 +78,14 @@ def test_workspace_queries(lib):
 def test_call_workspace_query_follows_the_launch_shape(lib):
     """The per-call query gives the partial rows of the launch shape the call
     takes: 12 warps per SM (1824 target units) for the "bf16" policy with a
-    bias and documents of 32 tokens or more on average, 16 warps (2432)
-    otherwise; never more than the policy's query."""
+    bias and documents of 32 tokens or more on average and for shorter
+    documents, 16 warps (2432) without a bias on longer documents; never more
+    than the policy's query."""
     S, C, row = 65536, 6144, 128 * 5 * 4
     call = vcd.conv1d_bwd_call_workspace_size
     assert call(S, C, 20, "bf16", True) == 48 * 38 * row           # wide: 1824 units
     assert call(S, C, 20, "bf16", False) == 48 * 50 * row          # deep: 2400 units
-    assert call(S, C, S // 32, "bf16", True) == 48 * 50 * row      # short documents: deep
+    assert call(S, C, S // 32, "bf16", True) == 48 * 38 * row      # short documents: chunked
     assert call(S, C, S // 32 - 1, "bf16", True) == 48 * 38 * row
     assert call(S, C, 20, "fp32", True) == call(S, C, 20, "fp32", False) == 48 * 38 * row  # chunks
     for S_, C_, nd in ((4096, 256, 4), (131072, 1032, 52000), (300, 40, 3), (1, 8, 1)):
@@ -182,9 +183,9 @@ def test_binding_rejects_host_tensors_before_any_call():
 def test_workspace_queries_are_consistent(lib):
     """Random shapes: the per-call need is a whole number of 2560-byte partial
     rows, never above its policy's need, which is never above the need of every
-    route; the "bf16" policy's need is the larger of its launch shapes' needs
-    (16 warps for short documents or no bias, 12 warps with a bias), and the
-    "fp32" policy always takes the same (chunked) shape."""
+    route; the "bf16" policy's need is the largest of its launch shapes' needs
+    (16 warps without a bias, 12 warps with a bias or on short documents), and
+    the "fp32" policy always takes the same (chunked) shape."""
     rng = np.random.default_rng(2024)
     call = vcd.conv1d_bwd_call_workspace_size
     for _ in range(300):
@@ -201,7 +202,8 @@ def test_workspace_queries_are_consistent(lib):
             if pol == "fp32":
                 assert call(S, C, nd, pol, True) == call(S, C, 1, pol, False) == route
             elif S > 32:
-                assert route == max(call(S, C, 1, pol, True), call(S, C, 1, pol, False))
+                assert route == max(call(S, C, 1, pol, True), call(S, C, 1, pol, False),
+                                    call(S, C, S, pol, True))
         assert total == max(vcd.conv1d_bwd_route_workspace_size(S, C, p) for p in ("bf16", "fp32"))
 
 

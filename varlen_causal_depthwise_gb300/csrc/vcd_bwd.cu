@@ -1199,14 +1199,20 @@ cudaError_t launch_bwd(const BwdArgs& args, int sm_count, cudaStream_t stream) {
     static const L wide_bf16[2][3] = {
         {nullptr, launch_main_t<kBwdWide, false, kBiasF32, kPolicyBF16>, launch_main_t<kBwdWide, false, kBiasBF16, kPolicyBF16>},
         {nullptr, launch_main_t<kBwdWide, true, kBiasF32, kPolicyBF16>, launch_main_t<kBwdWide, true, kBiasBF16, kPolicyBF16>}};
-    static const L deep_bf16[2][3] = {VCD_ROW(kBwdDeep, false, kPolicyBF16), VCD_ROW(kBwdDeep, true, kPolicyBF16)};
+    // The deep shape serves "bf16"-policy calls without a bias on longer
+    // documents only; the chunked one "fp32" calls and short documents.
+    static const L deep_bf16[2][3] = {{launch_main_t<kBwdDeep, false, kBiasNone, kPolicyBF16>, nullptr, nullptr},
+                                      {launch_main_t<kBwdDeep, true, kBiasNone, kPolicyBF16>, nullptr, nullptr}};
+    static const L chunked_bf16[2][3] = {VCD_ROW(kBwdChunked, false, kPolicyBF16),
+                                         VCD_ROW(kBwdChunked, true, kPolicyBF16)};
     static const L fp32_t[2][3] = {VCD_ROW(kBwdChunked, false, kPolicyFP32),
                                    VCD_ROW(kBwdChunked, true, kPolicyFP32)};
 #undef VCD_ROW
     const int wi = a.weight_bf16 ? 1 : 0;
     const bool fp32 = a.policy == kPolicyFP32;
     const L fn = fp32 ? (a.shape == kBwdChunked ? fp32_t[wi][a.bias_kind] : nullptr)
-                      : a.shape == kBwdWide ? wide_bf16[wi][a.bias_kind] : deep_bf16[wi][a.bias_kind];
+                      : a.shape == kBwdWide ? wide_bf16[wi][a.bias_kind]
+                      : a.shape == kBwdChunked ? chunked_bf16[wi][a.bias_kind] : deep_bf16[wi][a.bias_kind];
     if (fn == nullptr) return cudaErrorInvalidValue;     // a shape bwd_shape never picks
     cudaError_t e = fn(a, sm_count, stream);
     if (e != cudaSuccess) return e;

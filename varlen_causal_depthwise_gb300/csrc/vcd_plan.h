@@ -56,13 +56,13 @@ enum FwdShape { kFwdStream = 0, kFwdShortDocs = 1, kFwdExact = 2 };
 // warps.
 //   kBwdWide: 12 warps, up to 168 registers a thread -- mask-free streaming
 //             whose 16-warp build would spill;
-//   kBwdDeep: 16 warps, up to 128 registers a thread -- more warps to hide the
-//             latency of instruction-heavy paths (document masks in most
-//             batches, the "fp32" policy's SiLU').
+//   kBwdDeep: 16 warps, up to 128 registers a thread -- more warps to hide
+//             latency, for the mask-free routes without a bias.
 // bwd_shape() picks one per call.
 //   kBwdChunked: 12 warps, up to 168 registers, 8-token batches and room in
 //             shared memory for compensated per-chunk sums -- the "fp32"
-//             policy's chunks of units of at most 256 tokens.
+//             policy's chunks of units of at most 256 tokens, and short
+//             documents (masked paths) under either policy.
 enum BwdShape { kBwdWide = 0, kBwdDeep = 1, kBwdChunked = 2 };
 constexpr int kBwdShapeWarps[3] = {12, 16, 12};
 
@@ -76,16 +76,15 @@ inline int fwd_shape(int64_t S, int64_t num_docs) {
 }
 
 // The backward's launch shape for a call: chunked for the "fp32" policy (its
-// short units need the shared-memory chunk sums); under the "bf16"
-// policy deep for short documents (instruction-heavy masked paths, where more
-// warps hide more latency) and for routes without a bias (those kernels keep
-// all their state within 128 registers), wide with a bias on longer
-// documents, whose 16-warp kernels would spill. A function of the call's
-// arguments only, so a route's partial rows are the same on every call and
-// every device.
+// short units need the shared-memory chunk sums) and for short documents
+// (the masked interior path without the deep shape's spills: 131072 x 1032
+// 174.7 -> 172.7 us, measured); under the "bf16" policy on longer documents
+// deep for routes without a bias (those kernels keep all their state within
+// 128 registers), wide with a bias, whose 16-warp kernels would spill. A
+// function of the call's arguments only, so a route's partial rows are the
+// same on every call and every device.
 inline int bwd_shape(int64_t S, int64_t num_docs, int policy, bool has_bias) {
-    if (policy == 1) return kBwdChunked;
-    if (num_docs * kShortDocTokens >= S) return kBwdDeep;
+    if (policy == 1 || num_docs * kShortDocTokens >= S) return kBwdChunked;
     return has_bias ? kBwdWide : kBwdDeep;
 }
 
@@ -278,7 +277,9 @@ inline uint64_t bwd_workspace_bytes_for(int64_t S, int64_t C, int policy) {
     if (policy == 1) return bwd_workspace_bytes_for(S, C, policy, kBwdChunked);
     const uint64_t d = bwd_workspace_bytes_for(S, C, policy, kBwdDeep);
     const uint64_t w = bwd_workspace_bytes_for(S, C, policy, kBwdWide);
-    return w > d ? w : d;
+    const uint64_t c = bwd_workspace_bytes_for(S, C, policy, kBwdChunked);
+    const uint64_t m = w > d ? w : d;
+    return c > m ? c : m;
 }
 
 // What one call needs.
