@@ -273,6 +273,7 @@ def test_recipes_full_size_sampled(name):
 @pytest.mark.parametrize("S,C,docs,bias", [
     (8000, 8200, ("uniform", 1, 3000, 0), torch.float32),    # "fp32": chunks of 2 units
     (8000, 8200, ("uniform", 0, 5, 0), None),                # short documents, no bias
+    (16000, 1032, ("uniform", 100, 2000, 0), None),          # long documents, no bias: deep shape
     (30000, 2056, ("uniform", 0, 2000, 3), torch.bfloat16),  # "fp32": 14 transposed warps
     (20000, 72, ("uniform", 0, 300, 1), torch.float32),      # 18 groups: not transposed
     (20000, 40, ("uniform", 0, 9, 2), torch.float32),        # one column of 10 groups
