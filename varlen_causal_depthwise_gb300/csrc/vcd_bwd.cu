@@ -942,16 +942,21 @@ __global__ void __launch_bounds__(kRedOutputs * kRedMaxSlices, 4) bwd_reduce_ker
 
 // ------------------------------------------------------- exact fix-up ---
 
-// First token of the document holding t (the last cu_seqlens entry <= t);
-// clamped so that a malformed array cannot send a read out of range.
-__device__ int64_t doc_start_of(const int32_t* __restrict__ cu, int ncu, int64_t t) {
+// The document holding t: its first token s0 (the last cu_seqlens entry
+// <= t) and the first token past t where another document starts (the first
+// entry > t; no such entry: S). Token j > t is in t's document iff j < next.
+// Clamped so that a malformed array cannot send a read out of range.
+__device__ void doc_of(const int32_t* __restrict__ cu, int ncu, int64_t t, int64_t S, int64_t& s0,
+                       int64_t& next) {
     int lo = 0, hi = ncu;                                   // cu[lo] <= t < cu[hi] when sorted
     while (hi - lo > 1) {
         const int mid = lo + (hi - lo) / 2;
         if ((int64_t)__ldg(cu + mid) <= t) lo = mid; else hi = mid;
     }
     const int64_t s = __ldg(cu + lo);
-    return s < 0 ? 0 : s > t ? t : s;
+    s0 = s < 0 ? 0 : s > t ? t : s;
+    const int64_t n = hi < ncu ? (int64_t)__ldg(cu + hi) : S;
+    next = n > t ? n : t + 1;
 }
 
 __device__ float param_at(const void* base, bool bf16, int64_t i) {
@@ -974,11 +979,12 @@ __device__ __nv_bfloat16 dx_exact(const BwdArgs& a, int64_t t, int64_t c) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) wk[k] = param_at(a.weight, wb, c * 4 + k);
     const float bias = a.bias_kind == kBiasNone ? 0.0f : param_at(a.bias, a.bias_kind == kBiasBF16, c);
-    const int64_t s0 = doc_start_of(cu, ncu, t);
+    int64_t s0, next;
+    doc_of(cu, ncu, t, S, s0, next);
     dfloat acc = df_of(0.0f);
     for (int k = 0; k < 4; ++k) {
         const int64_t j = t + 3 - k;                         // the token whose pre used x[t] via tap k
-        if (j >= S || doc_start_of(cu, ncu, j) != s0) continue;
+        if (j >= S || j >= next) continue;                   // past the end, or in a later document
         float xs[4];
         bool on[4];
 #pragma unroll
