@@ -58,7 +58,7 @@ FALLBACK_HBM_GBS = 6800.0
 # kernel reports traffic null until it is profiled again. Taken on the same
 # workload at S = 16384 (a capture small enough for ncu's replay) and scaled by
 # the 4x units of S = 65536 (traffic is proportional to tokens).
-NCU_TRAFFIC = {"f6123f10279346cb": 4 * 579.220224e6}
+NCU_TRAFFIC = {"23535773b6930b8c": 4 * 579.377408e6}
 KERNEL_SOURCES = ["varlen_causal_depthwise_gb300/csrc/vcd_bwd.cu",
                   "varlen_causal_depthwise_gb300/csrc/vcd_device.cuh",
                   "varlen_causal_depthwise_gb300/csrc/vcd_dfloat.cuh",
