@@ -42,7 +42,10 @@ constexpr int kFwdColCh = 32 * kFwdVec;               // channels per unit colum
 constexpr int kFwdRowBytes = 2 * kFwdColCh;            // bytes of a token's row segment
 
 // Batch geometry of a forward shape (vcd_plan.h): tokens per batch and ring
-// stages.
+// stages. Short documents take 16-token batches in 2 stages: their per-batch
+// cu_seqlens walk and masks are the cost, so fewer, longer batches pay
+// (131072 x 1032: 8 x 3 104.5 us, 8 x 4 106.6, 12 x 3 104.3, 16 x 2 100.4;
+// measured).
 // kTma: the stages arrive by tensor-map copies (one per batch, issued by one
 // lane, onto an mbarrier) instead of per-lane cp.async -- faster where most
 // batches walk cu_seqlens and take the masked path (short documents: 110 ->
@@ -55,7 +58,7 @@ template <> struct FwdGeom<kFwdStream> {
     static constexpr int kU = 4, kNs = 6, kCtas = kFwdCtasPerSm; static constexpr bool kTma = false;
 };
 template <> struct FwdGeom<kFwdShortDocs> {
-    static constexpr int kU = 8, kNs = 3, kCtas = kFwdCtasPerSm; static constexpr bool kTma = true;
+    static constexpr int kU = 16, kNs = 2, kCtas = kFwdCtasPerSm; static constexpr bool kTma = true;
 };
 template <> struct FwdGeom<kFwdExact> {
     static constexpr int kU = 8, kNs = 3, kCtas = 2; static constexpr bool kTma = true;

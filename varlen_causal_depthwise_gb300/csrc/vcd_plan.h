@@ -45,8 +45,8 @@ constexpr int64_t kFwdTargetUnits = kGb300Sms * kFwdCtasPerSm * kWarpsPerCta;
 // Forward batch shapes: the same units and grid, different batches. Streaming
 // takes 4-token batches in a 6-stage ring; short documents (a start in most
 // batches, so each batch walks cu_seqlens and takes the masked path) take
-// 8-token batches in a 3-stage ring, which halves those per-batch costs. The
-// choice changes no result, only the time.
+// 16-token batches in a 2-stage ring, which quarters those per-batch costs.
+// The choice changes no result, only the time.
 // kFwdExact is the exactness-guarded route (conv1d_fwd_exact): 8-token
 // batches on every workload, each element checked and the doubtful ones
 // recomputed (vcd_fwd.cu).
