@@ -6,9 +6,11 @@
 // with zero history before each document's first token.
 //
 // One warp per work unit (128 channels x L tokens, vcd_plan.h); a lane owns 4
-// channels (kFwdVec). The warp streams its 256-byte row segments into a shared-memory
-// ring with cp.async, kFwdNs - 1 batches of kFwdU tokens ahead of the
-// arithmetic, so the loads in flight cost no registers. The three previous
+// channels (kFwdVec). The warp streams its 256-byte row segments into a
+// shared-memory ring, kFwdNs - 1 batches of kFwdU tokens ahead of the
+// arithmetic, so the loads in flight cost no registers: per-lane 16-byte
+// cp.async in the streaming shape, one tensor-map copy (TMA) per batch onto
+// the stage's mbarrier for short documents and the exact route. The three previous
 // tokens of x stay in registers as FP32. Document starts come from a warp-wide
 // walk over cu_seqlens as one bit mask per batch (positions q-2 .. q+U-1); a
 // batch with no start in it takes a mask-free path, otherwise each tap is
