@@ -83,11 +83,13 @@ int conv1d_bwd_route_workspace_size(int64_t S, int64_t C, int policy, size_t* by
 /* Bytes of backward workspace one call needs, exactly (backward page,
  * Parameters: workspace): the partial rows that
  * conv1d_bwd writes and reads for these arguments (has_bias: a bias is
- * passed). The call picks one of three launch shapes from them -- for the
- * "bf16" policy 16 warps per SM when documents are shorter than 32 tokens on
- * average (num_docs * 32 >= S) or there is no bias, 12 warps with more
- * registers otherwise; for the "fp32" policy 12 warps with shared memory for
- * its chunk sums -- and the shape sets the number of chunks. At most
+ * passed). The call picks one of three launch shapes from them -- 12 warps
+ * per SM with shared memory for chunk sums for the "fp32" policy and, under
+ * either policy, when documents are shorter than 32 tokens on average
+ * (num_docs * 32 >= S); otherwise under "bf16" 16 warps per SM without a
+ * bias, 12 warps with more registers with one -- and the shape and C (a last
+ * 128-channel column with at most 64 channels is transposed) set the number
+ * of chunks. At most
  * conv1d_bwd_route_workspace_size(S, C, policy). Errors as
  * conv1d_bwd_route_workspace_size, plus VCD_ERR_INVALID_ARG for S > 0 with
  * num_docs <= 0. */
